@@ -1,0 +1,152 @@
+"""Seeded synthetic inputs for the fused exact-attention forward.
+
+This module is shared by the oracle's tests, the GPU parity tests, ``bench.py`` and the smoke
+check.  It holds no attention arithmetic: only the workload table, random draws, rounding of the
+draws to the operand dtype, the per-tensor fp8 input quantisation and the choice of sampled rows.
+
+Input recipe (the same bytes go to the CUDA path and to the oracle):
+
+* ``torch.Generator('cpu').manual_seed(seed)``; then ``randn`` fp32 for Q, then K, then V, each of
+  shape ``[B, H, N, d]`` (head dim contiguous), in that order.
+* bf16 operands: round-to-nearest-even of the fp32 draw (``Tensor.to(torch.bfloat16)``).  A
+  ``q_mult`` (a power of two) is applied after the rounding, so it is exact.
+* fp8-e4m3 operands: per-tensor descale ``amax(|X|) / 448`` (the format's largest finite value)
+  and ``X_q = e4m3(RNE(X / descale))`` as in the per-tensor scaling of the FlashAttention
+  explainer page (section 3.3.3 "Scaling").  The kernel and the oracle both receive ``X_q`` and the
+  descale; the quantisation error itself is not part of the comparison.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+E4M3_MAX = 448.0
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One attention-forward problem: shapes, mask, operand dtype and seed."""
+
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    causal: bool
+    dtype: str  # "bf16" or "e4m3"
+    seed: int
+    q_mult: float = 1.0
+    note: str = field(default="", compare=False)
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def flops(self) -> float:
+        """4·B·H·N²·d, halved for the causal mask (the usual attention-forward convention)."""
+        f = 4.0 * self.B * self.H * self.N * self.N * self.d
+        return f / 2 if self.causal else f
+
+    @property
+    def rows(self) -> int:
+        return self.B * self.H * self.N
+
+    def describe(self) -> str:
+        mask = "causal" if self.causal else "non-causal"
+        qm = f" Q*{self.q_mult:g}" if self.q_mult != 1.0 else ""
+        return f"B{self.B} H{self.H} N{self.N} d{self.d} {self.dtype} {mask}{qm}"
+
+
+# The five benchmark shapes of the method (plus the Q*8 stress variant of the causal one).
+WORKLOADS = {
+    "b1h1n256d64_bf16": Workload("b1h1n256d64_bf16", 1, 1, 256, 64, False, "bf16", 1000,
+                                 note="small case the oracle finishes in well under a second"),
+    "b4h16n2048d128_bf16_causal": Workload("b4h16n2048d128_bf16_causal", 4, 16, 2048, 128, True,
+                                           "bf16", 1001),
+    "b4h16n2048d128_bf16_causal_q8": Workload("b4h16n2048d128_bf16_causal_q8", 4, 16, 2048, 128,
+                                              True, "bf16", 1001, q_mult=8.0,
+                                              note="logits spread over about +-100"),
+    "b2h32n8192d128_bf16": Workload("b2h32n8192d128_bf16", 2, 32, 8192, 128, False, "bf16", 1002,
+                                    note="headline throughput shape"),
+    "b1h16n32768d64_bf16_causal": Workload("b1h16n32768d64_bf16_causal", 1, 16, 32768, 64, True,
+                                           "bf16", 1003, note="long sequence"),
+    "b2h32n16384d128_e4m3": Workload("b2h32n16384d128_e4m3", 2, 32, 16384, 128, False, "e4m3",
+                                     1004, note="fp8 operands, per-tensor descale"),
+}
+
+HEADLINE = "b2h32n8192d128_bf16"
+
+
+@dataclass
+class Inputs:
+    """Operands on the host.  ``q``/``k``/``v`` are bf16 or float8_e4m3fn CPU tensors."""
+
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    descale_q: float = 1.0
+    descale_k: float = 1.0
+    descale_v: float = 1.0
+
+    @property
+    def dtype(self) -> str:
+        return "e4m3" if self.q.dtype == torch.float8_e4m3fn else "bf16"
+
+    def raw(self, name: str):
+        """The operand's bytes as a numpy array (uint16 for bf16, uint8 for e4m3)."""
+        t = getattr(self, name).contiguous()
+        if t.dtype == torch.bfloat16:
+            return t.view(torch.int16).numpy().view("uint16")
+        return t.view(torch.uint8).numpy()
+
+
+def quantize_e4m3(x: torch.Tensor):
+    """Per-tensor fp8 quantisation: returns (e4m3 tensor, fp32 descale)."""
+    amax = float(x.abs().max())
+    descale = amax / E4M3_MAX if amax > 0 else 1.0
+    xq = (x / torch.tensor(descale, dtype=torch.float32)).to(torch.float8_e4m3fn)
+    return xq, descale
+
+
+def random_inputs(B: int, H: int, N: int, d: int, dtype: str = "bf16", seed: int = 0,
+                  q_mult: float = 1.0) -> Inputs:
+    """iid N(0,1) draws for Q, K, V in that order, rounded to the operand dtype."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    shape = (B, H, N, d)
+    q = torch.randn(shape, generator=g, dtype=torch.float32)
+    k = torch.randn(shape, generator=g, dtype=torch.float32)
+    v = torch.randn(shape, generator=g, dtype=torch.float32)
+    if dtype == "bf16":
+        qb = q.to(torch.bfloat16)
+        if q_mult != 1.0:
+            qb = qb * q_mult
+        return Inputs(qb, k.to(torch.bfloat16), v.to(torch.bfloat16))
+    if dtype == "e4m3":
+        if q_mult != 1.0:
+            q = q * q_mult
+        qq, dq = quantize_e4m3(q)
+        kq, dk = quantize_e4m3(k)
+        vq, dv = quantize_e4m3(v)
+        return Inputs(qq, kq, vq, dq, dk, dv)
+    raise ValueError(f"unknown operand dtype {dtype!r}")
+
+
+def make_inputs(w: Workload) -> Inputs:
+    return random_inputs(w.B, w.H, w.N, w.d, w.dtype, w.seed, w.q_mult)
+
+
+def sample_rows(N: int, seed: int, extra: int = 56):
+    """Deterministic query rows checked one by one at full size: tile edges plus seeded picks."""
+    fixed = {0, 1, 2, 127, 128, 255, 256, N - 1}
+    rows = {r for r in fixed if 0 <= r < N}
+    g = torch.Generator(device="cpu").manual_seed(seed + 7777)
+    if N > len(rows):
+        pick = torch.randperm(N, generator=g)[: extra + len(rows)].tolist()
+        for r in pick:
+            if len(rows) >= len(fixed) + extra:
+                break
+            rows.add(int(r))
+    return sorted(rows)
