@@ -1,0 +1,370 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused attention forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step is one attention forward (the whole hot path: one kernel launch) over one batch of
+seeded synthetic inputs already resident in HBM.  The default workload is the headline shape
+B=2, H=32, N=8192, d=128, bf16, non-causal; every input tensor (134 MB each, 403 MB for Q, K, V)
+is larger than the 129 MB L2, so consecutive steps do not find their inputs in L2.
+
+Prints ONE JSON line on rank 0: the metric (attention forward TFLOPS, 4·B·H·N²·d, halved for
+the causal mask), the device-timed value, an end-to-end value through the C ABI with host
+buffers (H2D of Q, K, V and D2H of O, LSE inside the timed region), the roofline of the kernel
+against the measured peak, SM clocks sampled during the timed region, and the fp64 CPU oracle
+timed on a bounded sample of the same workload.  ``--impl reference`` times that oracle as the
+reference arm instead.  Under torchrun every rank runs its own copy of the workload (independent
+(batch, head) problems: weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import HEADLINE, WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "attention fwd TFLOPS and % of GB300 dense BF16/FP8 peak (1 GPU, device-timed)"
+UNIT = "TFLOPS"
+FP8_OVER_BF16 = 4.5 / 2.25          # nominal dense fp8 : bf16 tensor ratio
+EXP_PER_CLK_SM = 32                 # measured MUFU ex2 rate on this GB300 (probe)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16": float(p["bf16_tflops"]), "bf16_sustained": float(p["bf16_tflops_sustained"]),
+                "hbm_gbs": float(p["hbm_gbs"]), "source": "measured"}
+    return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling in the background during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"exattn_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, busy_fraction: float = 0.5):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        pmax = max(r[2] for r in rows)
+        loaded = [r for r in rows if r[2] >= busy_fraction * pmax] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3])
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded),
+                "sm_max_mhz": max(r[1] for r in loaded),
+                "power_w_max": pmax, "samples": len(loaded), "reasons": reasons}
+
+
+def oracle_sample_rate(inp, w, target_s: float, seed: int = 0):
+    """Time the fp64 oracle on a sample of rows sized for about target_s; return TFLOPS-equiv."""
+    from oracle import oracle
+
+    orc = oracle.get()
+    cores = os.cpu_count() or 1
+    heads = min(w.B * w.H, 4)
+    sub = type(inp)(inp.q[:1, :heads], inp.k[:1, :heads], inp.v[:1, :heads],
+                    inp.descale_q, inp.descale_k, inp.descale_v) if w.B * w.H > 1 else inp
+    rng_rows = list(range(w.N - 1, -1, -max(1, w.N // 4096)))  # spread over the sequence
+
+    def run(nrows):
+        rows = sorted(rng_rows[:nrows])
+        t0 = time.perf_counter()
+        orc.attention_fwd(sub.raw("q"), sub.raw("k"), sub.raw("v"), w.scale, w.causal, sub.dtype,
+                          (sub.descale_q, sub.descale_k, sub.descale_v), rows, cores)
+        dt = time.perf_counter() - t0
+        keys = sum((r + 1) if w.causal else w.N for r in rows)
+        flops = 4.0 * keys * w.d * sub.q.shape[1]
+        return flops, dt, len(rows)
+
+    n = min(len(rng_rows), 64)
+    flops, dt, nr = run(n)
+    if dt < target_s:
+        n = min(len(rng_rows), max(n, int(n * target_s / max(dt, 1e-3))))
+        flops, dt, nr = run(n)
+    sample = (f"{nr} query rows x {sub.q.shape[1]} heads of {w.name} "
+              f"({'causal' if w.causal else 'all'} keys each), fp64")
+    return flops / dt / 1e12, dt, cores, sample
+
+
+KERNEL_SOURCES = ["exact_attention_13_gb300/csrc/fa_fwd_kernel.cuh",
+                  "exact_attention_13_gb300/csrc/sm103_ptx.cuh",
+                  "exact_attention_13_gb300/csrc/fa_api.cu"]
+
+
+def kernel_sources_sha256() -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str, override):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on these sources."""
+    if override is not None:
+        return override
+    path = os.path.join(ROOT, "profiles", "fa_fwd_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    ent = rec.get(workload)
+    if not ent or ent.get("kernel_sources_sha256") != kernel_sources_sha256():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def init_dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if _cuda_ok() else "gloo")
+    return world, rank, local
+
+
+def _cuda_ok():
+    import torch
+
+    return torch.cuda.is_available()
+
+
+def run_reference(args, w, world, rank):
+    """Reference arm: the fp64 CPU oracle as it stands, on bounded samples of the workload."""
+    if rank != 0:
+        return
+    inp = make_inputs(w)
+    rates, times = [], []
+    cores, sample = None, None
+    for step in range(args.warmup + args.steps):
+        tf, dt, cores, sample = oracle_sample_rate(inp, w, target_s=args.ref_step_s)
+        if step >= args.warmup:
+            rates.append(tf)
+            times.append(dt)
+    value = statistics.median(rates)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * statistics.median(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "shape": w.describe(), "parallelism": "host threads"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w, world, rank, local):
+    import torch
+
+    import exact_attention_13_gb300 as ea
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device for --impl ours")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    inp = make_inputs(w)
+    q, k, v = (getattr(inp, n).to(dev) for n in "qkv")
+    descale = (inp.descale_q, inp.descale_k, inp.descale_v)
+    o = torch.empty(w.B, w.H, w.N, w.d, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ea.fwd(q, k, v, causal=w.causal, scale=w.scale, descale=descale, out=o, lse=lse)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    # ---- device-timed region: K launches back to back on one stream
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    ms = start.elapsed_time(end) / args.steps
+    clocks = clk.summary()
+    ms_max = ms
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    assert ea.device_status() == 0, "device wait timed out during the bench"
+
+    # ---- end to end: pinned host inputs -> device -> attention -> host outputs
+    qh, kh, vh = (getattr(inp, n).pin_memory() for n in "qkv")
+    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step():
+        q.copy_(qh, non_blocking=True)
+        k.copy_(kh, non_blocking=True)
+        v.copy_(vh, non_blocking=True)
+        step()
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    e_ms = e_start.elapsed_time(e_end) / args.steps
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e_ms = float(t.item())
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+
+    flops_rank = w.flops
+    value = world * flops_rank / (ms_max * 1e-3) / 1e12
+    e2e_value = world * flops_rank / (e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        return
+    pk = peaks()
+    is_fp8 = w.dtype == "e4m3"
+    peak = pk["bf16"] * (FP8_OVER_BF16 if is_fp8 else 1.0)
+    achieved = flops_rank / (ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": measured_traffic(w.name, args.traffic_bytes),
+                "peak_kind": (f"{pk['source']} cuBLAS bf16 burst"
+                              + (" x 2 (nominal fp8:bf16)" if is_fp8 else "")),
+                "kernel": "exattn::fa_fwd_kernel"}
+    # exp-unit bound at the clock seen during the run (informative)
+    exps = w.B * w.H * (w.N * (w.N + 1) / 2 if w.causal else w.N * w.N)
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = clocks.get("sm_mhz") or 2070.0
+    exp_floor_ms = exps / (EXP_PER_CLK_SM * sm_count * mhz * 1e6) * 1e3
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if is_fp8 else "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "shape": w.describe(), "global_batch": w.B * world,
+                   "heads": w.H, "seq_len": w.N, "head_dim": w.d, "causal": w.causal,
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (no flush)" if 3 * q.numel() * q.element_size()
+                   > 129e6 else "inputs smaller than L2"},
+        "pct_of_peak": 100.0 * achieved / peak,
+        "exp_bound": {"exp_per_clk_sm": EXP_PER_CLK_SM, "floor_ms": exp_floor_ms,
+                      "frac": exp_floor_ms / ms},
+        "roofline": roofline,
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms},
+        "gpu_launches": args.steps,
+    }
+    if not args.no_cpu_baseline:
+        tf, dt, cores, sample = oracle_sample_rate(inp, w, target_s=args.cpu_s)
+        line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": sample, "seconds": dt}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-s", type=float, default=12.0, help="seconds of oracle work")
+    ap.add_argument("--ref-step-s", type=float, default=4.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic-bytes", type=float, default=None,
+                    help="DRAM bytes per launch from an ncu capture of the current kernel")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        # host-only arm: no process group; under torchrun rank 0 alone does the work
+        run_reference(args, w, int(os.environ.get("WORLD_SIZE", "1")),
+                      int(os.environ.get("RANK", "0")))
+        return
+    world, rank, local = init_dist()
+    run_ours(args, w, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,175 @@
+"""exact_attention_13_gb300 -- fused exact-attention forward on GB300 (sm_103a).
+
+A thin ctypes binding over ``libexattn.so`` (C ABI in ``include/exact_attention.h``).  This
+module only checks and marshals arguments; every step of the attention forward runs in the
+library's CUDA kernel.  PyTorch supplies device memory and the current stream.  There is no
+fallback: if the library is missing or fails to load, importing ``lib()`` raises.
+
+    import exact_attention_13_gb300 as ea
+    o, lse = ea.fwd(q, k, v, causal=True)           # q, k, v: [B, H, N, d] bf16 on cuda
+    o, lse = ea.fwd(q8, k8, v8, descale=(dq, dk, dv))  # float8_e4m3fn operands
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+from . import _build
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_MISALIGNED = 3
+FA_ERR_CUDA = 4
+FA_ERR_DEVICE_TIMEOUT = 5
+FA_DTYPE_BF16 = 0
+FA_DTYPE_FP8_E4M3 = 1
+
+LIB_PATH = _build.LIB_PATH
+
+# every entry point of include/exact_attention.h: (restype, argtypes)
+_c = ctypes
+SIGNATURES = {
+    "fa_fwd": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                          _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_float, _c.c_int, _c.c_int,
+                          _c.c_void_p]),
+    "fa_fwd_ex": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                             _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_float, _c.c_int,
+                             _c.c_int, _c.c_void_p, _c.c_void_p]),
+    "fa_device_status": (_c.c_int, [_c.c_int, _c.POINTER(_c.c_int)]),
+    "fa_status_string": (_c.c_char_p, [_c.c_int]),
+    "fa_version": (_c.c_int, []),
+    "fa_debug_exp2": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_longlong, _c.c_int,
+                                 _c.c_void_p]),
+}
+
+
+class FwdOpts(ctypes.Structure):
+    """Mirror of ``fa_fwd_opts``."""
+
+    _fields_ = [("descale_q", ctypes.c_float), ("descale_k", ctypes.c_float),
+                ("descale_v", ctypes.c_float), ("dev_status", ctypes.c_void_p)]
+
+
+class AttentionError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        msg = _status_name(code)
+        super().__init__(f"{what}: {msg} (status {code})" if what else f"{msg} (status {code})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib(path: str | None = None) -> ctypes.CDLL:
+    """The loaded library (built first if the sources are newer).  Raises if it cannot load."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIB_PATH
+            if path is None and not _build.up_to_date():
+                _build.build()
+            if not os.path.exists(p):
+                raise ImportError(f"libexattn.so not found at {p}; run the build first")
+            handle = ctypes.CDLL(p)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = handle
+        return _lib
+
+
+def _status_name(code: int) -> str:
+    try:
+        return lib().fa_status_string(code).decode()
+    except Exception:  # noqa: BLE001 -- message formatting only
+        return "status"
+
+
+def _check(code: int, what: str):
+    if code != FA_OK:
+        raise AttentionError(code, what)
+
+
+def fa_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, scale, causal, dtype, stream) -> int:
+    """Direct C-ABI call with raw device pointers; returns the status code."""
+    return lib().fa_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, scale, int(causal),
+                        dtype, stream)
+
+
+def fa_fwd_ex(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, scale, causal, dtype,
+              descale=(1.0, 1.0, 1.0), status_ptr=None, stream=None) -> int:
+    opts = FwdOpts(float(descale[0]), float(descale[1]), float(descale[2]), status_ptr)
+    return lib().fa_fwd_ex(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, scale, int(causal),
+                           dtype, ctypes.byref(opts), stream)
+
+
+def device_status(clear: bool = True) -> int:
+    out = ctypes.c_int(0)
+    _check(lib().fa_device_status(int(clear), ctypes.byref(out)), "fa_device_status")
+    return out.value
+
+
+def version() -> int:
+    return lib().fa_version()
+
+
+def fwd(q, k, v, causal: bool = False, scale: float | None = None, descale=None, out=None,
+        lse=None, status=None):
+    """Attention forward on torch CUDA tensors [B, H, N, d]; returns (o bf16, lse fp32).
+
+    ``descale`` = (dq, dk, dv) for float8_e4m3fn operands.  ``out``/``lse`` may be given
+    (contiguous, right shape and dtype) to avoid allocation.  ``status`` is an optional int32
+    CUDA tensor of one element the kernel sets to FA_ERR_DEVICE_TIMEOUT if a wait runs out.
+    """
+    import torch
+
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    if q.shape != k.shape or q.shape != v.shape or q.dim() != 4:
+        raise ValueError("q, k, v must share one [B, H, N, d] shape")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise ValueError("q, k, v must share one dtype")
+    if q.dtype == torch.bfloat16:
+        dtype = FA_DTYPE_BF16
+    elif q.dtype == torch.float8_e4m3fn:
+        dtype = FA_DTYPE_FP8_E4M3
+    else:
+        raise ValueError(f"unsupported operand dtype {q.dtype}")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
+    dq, dk, dv = descale if descale is not None else (1.0, 1.0, 1.0)
+    st = status.data_ptr() if status is not None else None
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    with torch.cuda.device(q.device):
+        rc = fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                       B, H, N, d, float(scale), causal, dtype, (dq, dk, dv), st, stream)
+    _check(rc, "fa_fwd_ex")
+    return out, lse
+
+
+def debug_exp2(x, mode: int):
+    """The kernel's 2^x routines on a CUDA float32 tensor (mode 0 MUFU, 1 FMA polynomial)."""
+    import torch
+
+    x = x.contiguous()
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream(x.device).cuda_stream
+    _check(lib().fa_debug_exp2(x.data_ptr(), y.data_ptr(), x.numel(), mode, stream),
+           "fa_debug_exp2")
+    return y

@@ -1,0 +1,216 @@
+// fa_api.cu -- host side of libexattn.so: argument checks, TMA tensor maps, kernel launch, and
+// the C ABI declared in include/exact_attention.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/exact_attention.h"
+#include "fa_fwd_kernel.cuh"
+
+namespace exattn {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Per-device status word the kernel writes when a bounded wait runs out (fa_fwd callers that
+// pass no status pointer of their own).
+__device__ int g_device_status;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Device-side address of g_device_status for the current device, looked up once per device.
+int* library_status_ptr(int dev) {
+  static std::atomic<int*> cache[kMaxDevices];
+  int* p = cache[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  void* addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) return nullptr;
+  cache[dev].store(static_cast<int*>(addr), std::memory_order_release);
+  return static_cast<int*>(addr);
+}
+
+// [B*H, N, d] view of one operand, tiles of 128 rows x (one swizzle span) with the swizzle the
+// MMA descriptors expect.  Rows past N (per head) read as zero.
+bool encode_operand_map(CUtensorMap* map, const void* ptr, int elem_bytes, int d, int n,
+                        int bh) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const int row_bytes = d * elem_bytes;
+  const int sw_bytes = row_bytes >= 128 ? 128 : row_bytes;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n),
+                        static_cast<cuuint64_t>(bh)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_bytes),
+                           static_cast<cuuint64_t>(row_bytes) * static_cast<cuuint64_t>(n)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(sw_bytes / elem_bytes), 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                       : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                  3, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  sw_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D, bool FP8, bool CAUSAL>
+int launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+           float c, float out_mult, int* status, cudaStream_t stream) {
+  constexpr int elem = FP8 ? 1 : 2;
+  CUtensorMap mq, mk, mv;
+  const int bh = B * H;
+  if (!encode_operand_map(&mq, q, elem, D, N, bh) || !encode_operand_map(&mk, k, elem, D, N, bh) ||
+      !encode_operand_map(&mv, v, elem, D, N, bh))
+    return FA_ERR_CUDA;
+  auto kern = fa_fwd_kernel<D, FP8, CAUSAL>;
+  constexpr int smem = smem_bytes<D, FP8>();
+  // one CTA per SM (the kernel takes all 512 TMEM columns): ask for > half the SM's smem
+  constexpr int smem_request = smem > 120 * 1024 ? smem : 120 * 1024;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  static std::atomic<uint64_t> attr_done{0};
+  if (!(attr_done.load(std::memory_order_acquire) & (1ull << dev))) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_request) !=
+        cudaSuccess)
+      return FA_ERR_CUDA;
+    attr_done.fetch_or(1ull << dev, std::memory_order_acq_rel);
+  }
+  KernelArgs args;
+  args.o = static_cast<__nv_bfloat16*>(o);
+  args.lse = lse;
+  args.status = status ? status : library_status_ptr(dev);
+  if (!args.status) return FA_ERR_CUDA;
+  args.n = N;
+  args.c = c;
+  args.out_mult = out_mult;
+  dim3 grid((N + kCtaRows - 1) / kCtaRows, bh, 1);
+  kern<<<grid, kThreads, smem_request, stream>>>(mq, mk, mv, args);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+template <int D, bool FP8>
+int launch_mask(int causal, const void* q, const void* k, const void* v, void* o, float* lse,
+                int B, int H, int N, float c, float om, int* st, cudaStream_t s) {
+  return causal ? launch<D, FP8, true>(q, k, v, o, lse, B, H, N, c, om, st, s)
+                : launch<D, FP8, false>(q, k, v, o, lse, B, H, N, c, om, st, s);
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+__global__ void exp2_probe_kernel(const float* x, float* y, long long n, int mode) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x)
+    y[i] = mode == 0 ? ex2_mufu(x[i]) : ex2_poly(x[i]);
+}
+
+}  // namespace
+}  // namespace exattn
+
+using namespace exattn;
+
+extern "C" {
+
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+              int N, int d, float scale, int causal, int dtype, const fa_fwd_opts* opts,
+              void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP8_E4M3) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
+  float dq = 1.f, dk = 1.f, dv = 1.f;
+  int* status = nullptr;
+  if (opts) {
+    status = opts->dev_status;
+    if (dtype == FA_DTYPE_FP8_E4M3) {
+      dq = opts->descale_q;
+      dk = opts->descale_k;
+      dv = opts->descale_v;
+      if (!std::isfinite(dq) || !std::isfinite(dk) || !std::isfinite(dv) || dq <= 0.f ||
+          dk <= 0.f || dv <= 0.f)
+        return FA_ERR_INVALID_ARG;
+    }
+  }
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H > 65535) return FA_ERR_UNSUPPORTED;
+  if (N > 0x7FFFFFFF - 2 * kCtaRows) return FA_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4) || (status && !aligned(status, 4)))
+    return FA_ERR_MISALIGNED;
+  const double c = static_cast<double>(scale) * 1.4426950408889634 * dq * dk;
+  if (!std::isfinite(c) || c > 3.0e38) return FA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const float cf = static_cast<float>(c);
+  if (dtype == FA_DTYPE_BF16) {
+    if (d == 64) return launch_mask<64, false>(causal, q, k, v, o, lse, B, H, N, cf, 1.f, status, s);
+    return launch_mask<128, false>(causal, q, k, v, o, lse, B, H, N, cf, 1.f, status, s);
+  }
+  if (d == 64) return launch_mask<64, true>(causal, q, k, v, o, lse, B, H, N, cf, dv, status, s);
+  return launch_mask<128, true>(causal, q, k, v, o, lse, B, H, N, cf, dv, status, s);
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+           int d, float scale, int causal, int dtype, void* stream) {
+  return fa_fwd_ex(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, nullptr, stream);
+}
+
+int fa_device_status(int clear, int* out) {
+  if (!out) return FA_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  if (clear) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess)
+      return FA_ERR_CUDA;
+  }
+  *out = v;
+  return FA_OK;
+}
+
+const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FA_ERR_MISALIGNED: return "misaligned pointer";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int fa_version(void) { return 100; }
+
+int fa_debug_exp2(const float* x, float* y, long long n, int mode, void* stream) {
+  if (!x || !y || n < 0 || (mode != 0 && mode != 1)) return FA_ERR_INVALID_ARG;
+  if (n == 0) return FA_OK;
+  long long blocks = (n + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  exp2_probe_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      x, y, n, mode);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,459 @@
+// fa_fwd_kernel.cuh -- fused exact-attention forward for sm_103a (tcgen05 + TMEM + TMA).
+//
+// One CTA owns 256 query rows of one (batch, head): two 128-row Q tiles, h = 0, 1.  It streams
+// the head's K/V in 128-row blocks through a ring of shared-memory slots and keeps, per row, the
+// online-softmax state (running max m, running sum l) in registers and the unnormalised output
+// in tensor memory ("FlashAttention · InkStack", sections 1.1.2 "Online Softmax" and 2.1; the
+// two-tile ping-pong and TMEM plan of "FlashAttention4 精读", section "新pipeline来overlap matmul
+// 和softmax").  Warp roles (384 threads):
+//
+//   warps 0-3  softmax, Q tile 0     one thread per query row: reads its S row from TMEM,
+//   warps 4-7  softmax, Q tile 1     updates (m, l), rescales its O row when m grew, writes the
+//                                    bf16/e4m3 probabilities back into the S columns, and at the
+//                                    end normalises O, stores it and the row's log-sum-exp
+//   warp  8    TMA producer          Q tiles once, then K_j, V_j into the ring (full/empty
+//                                    mbarriers, "FlashAttention · InkStack", section 3.2.1)
+//   warp  9    MMA issuer            one thread issues S_h = Q_h K_j^T (both operands in smem)
+//                                    and O_h += P_h V_j (P from TMEM, V from smem), and owns the
+//                                    TMEM allocation
+//   warps 10-11 idle
+//
+// TMEM (512 columns x 128 lanes, fp32 cells): S_0 at columns 0-127, S_1 at 128-255 (P_h is
+// written over S_h), O_0 at 256.., O_1 at 384.. .  Lane i holds row i of each tile.
+//
+// MMA issue order (tcgen05 MMAs from one thread execute in order):
+//   S0(0) S1(0) | PV0(0) S0(1) PV1(0) S1(1) | PV0(1) S0(2) PV1(1) S1(2) | ...
+// so the tensor core works on one tile while the other tile's softmax runs.  S_h(j+1) is issued
+// after PV_h(j), which makes it safe to overwrite P_h; the commit that signals S_h(j+1) also
+// proves PV_h(j) complete, so the softmax may rescale O_h right after it.
+//
+// Every mbarrier wait is bounded in time (globaltimer).  A wait that runs out sets a CTA-wide
+// abort flag and the status word; all roles then leave their loops, the MMA thread drains its
+// outstanding MMAs, the producer waits (bounded) for its outstanding copies, and the TMEM is
+// freed before the CTA exits.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "sm103_ptx.cuh"
+
+namespace exattn {
+
+constexpr int kThreads = 384;
+constexpr int kTileRows = 128;       // query rows per Q tile, keys per K/V block
+constexpr int kCtaRows = 2 * kTileRows;
+constexpr int kStatusTimeout = 5;    // FA_ERR_DEVICE_TIMEOUT
+constexpr uint64_t kWaitLimitNs = 4ull * 1000 * 1000 * 1000;  // 4 s per wait
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct KernelArgs {
+  __nv_bfloat16* o;   // [BH, N, d]
+  float* lse;         // [BH, N]
+  int* status;        // device status word (never null when launched by the library)
+  int n;              // keys = queries per head
+  float c;            // scale * log2(e) * descale_q * descale_k
+  float out_mult;     // descale_v (1 for bf16)
+};
+
+// Compile-time geometry of one instance.
+template <int D, bool FP8>
+struct Geo {
+  static constexpr int kElem = FP8 ? 1 : 2;                 // bytes per operand element
+  static constexpr int kRowBytes = D * kElem;               // bytes of one operand row
+  static constexpr int kSwBytes = kRowBytes >= 128 ? 128 : kRowBytes;  // swizzle span
+  static constexpr int kBoxes = kRowBytes / kSwBytes;       // TMA boxes per 128-row tile
+  static constexpr int kBoxElems = kSwBytes / kElem;        // inner box extent (elements)
+  static constexpr int kTileBytes = kTileRows * kRowBytes;  // one 128-row operand tile
+  static constexpr int kSlots = (FP8 || D == 64) ? 8 : 4;   // K/V ring depth
+  static constexpr int kQBytes = 2 * kTileBytes;
+  static constexpr int kRingBytes = kSlots * kTileBytes;
+  static constexpr uint32_t kSwMode = kSwBytes == 128 ? kSwizzle128B : kSwizzle64B;
+  static constexpr int kKStepBytes = 32;                    // K extent of one MMA, in bytes
+  static constexpr int kKStepsS = kRowBytes / kKStepBytes;  // MMAs per S = Q K^T
+  static constexpr int kKeysPerPv = FP8 ? 32 : 16;          // keys per PV MMA
+  static constexpr int kPvSteps = kTileRows / kKeysPerPv;   // MMAs per O += P V
+  static constexpr int kPCols = FP8 ? 32 : 64;              // TMEM columns of one P row
+  static constexpr uint32_t kIdescS = instr_desc(128, 128, FP8 ? 0 : 1, false, false);
+  static constexpr uint32_t kIdescPV = instr_desc(128, D, FP8 ? 0 : 1, false, true);
+};
+
+// Shared-memory control block (after the operand tiles).
+template <int kSlots>
+struct Ctrl {
+  uint64_t q_full;
+  uint64_t kv_full[kSlots];
+  uint64_t kv_empty[kSlots];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_full[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int D, bool FP8>
+constexpr int smem_bytes() {
+  using G = Geo<D, FP8>;
+  return G::kQBytes + G::kRingBytes + (int)sizeof(Ctrl<G::kSlots>) + 1024;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting or the wait ran out.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, int* abort_flag,
+                                           int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t spins = 0;
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++spins & 127u) == 0) {
+      if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *reinterpret_cast<volatile int*>(abort_flag) = 1;
+        atomicExch(status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// Key blocks Q tile h must visit: all of them, or (causal) those up to its diagonal block.
+// A tile whose first row is past the end of the sequence visits none.
+template <bool CAUSAL>
+__device__ __forceinline__ int kv_blocks_for_tile(int row0, int n) {
+  if (row0 >= n) return 0;
+  const int total = (n + kTileRows - 1) / kTileRows;
+  return CAUSAL ? (row0 / kTileRows + 1) : total;
+}
+
+template <int D, bool FP8, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                  const __grid_constant__ CUtensorMap map_v, const KernelArgs args) {
+  using G = Geo<D, FP8>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* s_q = smem;                          // two Q tiles
+  uint8_t* s_ring = smem + G::kQBytes;          // K/V slots
+  Ctrl<G::kSlots>* ctl = reinterpret_cast<Ctrl<G::kSlots>*>(s_ring + G::kRingBytes);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int n = args.n;
+  const int bh = blockIdx.y;
+  // heaviest query blocks first under the causal mask (they see the most keys)
+  const int mblock = CAUSAL ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x;
+  const int row0 = mblock * kCtaRows;
+  const int nkv0 = kv_blocks_for_tile<CAUSAL>(row0, n);
+  const int nkv1 = kv_blocks_for_tile<CAUSAL>(row0 + kTileRows, n);
+  const int nkv_load = nkv0 > nkv1 ? nkv0 : nkv1;
+
+  // ---------------------------------------------------------------- setup
+  if (warp == 9) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), 512);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&ctl->q_full), 1);
+    for (int s = 0; s < G::kSlots; ++s) {
+      mbar_init(smem_u32(&ctl->kv_full[s]), 1);
+      mbar_init(smem_u32(&ctl->kv_empty[s]), 1);
+    }
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(smem_u32(&ctl->s_full[h]), 1);
+      mbar_init(smem_u32(&ctl->p_full[h]), 4);  // one arrival per softmax warp
+      mbar_init(smem_u32(&ctl->o_full[h]), 1);
+    }
+    mbar_init(smem_u32(&ctl->drain), 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  int* abort_flag = &ctl->abort;
+
+  // registers: the producer/MMA warpgroup gives most of its share to the softmax warpgroups
+  // (384 threads x 168 at launch = 128 x (216 + 216 + 72))
+  if (warp >= 8) {
+    regs_dec<72>();
+  if (warp == 8) {
+    // ============================================================ TMA producer
+    if (lane == 0) {
+      tma_prefetch_map(&map_q);
+      tma_prefetch_map(&map_k);
+      tma_prefetch_map(&map_v);
+      const uint64_t keep = l2_policy_evict_last();   // K/V are re-read by other CTAs
+      const uint64_t once = l2_policy_evict_first();  // Q is read once
+      const uint32_t qbar = smem_u32(&ctl->q_full);
+      const int ntiles = (nkv0 > 0) + (nkv1 > 0);
+      if (ntiles > 0) {
+        mbar_arrive_expect_tx(qbar, ntiles * G::kTileBytes);
+        for (int h = 0; h < 2; ++h) {
+          if ((h == 0 ? nkv0 : nkv1) == 0) continue;
+          for (int b = 0; b < G::kBoxes; ++b)
+            tma_load_3d_hint(smem_u32(s_q + h * G::kTileBytes + b * kTileRows * G::kSwBytes),
+                             &map_q, qbar, b * G::kBoxElems, row0 + h * kTileRows, bh, once);
+        }
+      }
+      int issued = 0;
+      bool ok = true;
+      for (int t = 0; t < 2 * nkv_load && ok; ++t) {
+        const int slot = t % G::kSlots;
+        const int round = t / G::kSlots;
+        if (round > 0) {
+          ok = wait_phase(smem_u32(&ctl->kv_empty[slot]), (round - 1) & 1, abort_flag,
+                          args.status);
+          if (!ok) break;
+        }
+        const uint32_t fbar = smem_u32(&ctl->kv_full[slot]);
+        mbar_arrive_expect_tx(fbar, G::kTileBytes);
+        const CUtensorMap* map = (t & 1) ? &map_v : &map_k;
+        uint8_t* dst = s_ring + slot * G::kTileBytes;
+        for (int b = 0; b < G::kBoxes; ++b)
+          tma_load_3d_hint(smem_u32(dst + b * kTileRows * G::kSwBytes), map, fbar,
+                           b * G::kBoxElems, (t >> 1) * kTileRows, bh, keep);
+        ++issued;
+      }
+      if (!ok) {
+        // abort: let the copies already issued land before the CTA's smem goes away
+        if (ntiles > 0) wait_phase(smem_u32(&ctl->q_full), 0, abort_flag, args.status);
+        const int first = issued > G::kSlots ? issued - G::kSlots : 0;
+        for (int t = first; t < issued; ++t) {
+          const uint32_t fbar = smem_u32(&ctl->kv_full[t % G::kSlots]);
+          const uint32_t par = (t / G::kSlots) & 1;
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(fbar, par) && globaltimer_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ============================================================ MMA issuer
+    if (lane == 0 && nkv_load > 0) {
+      bool ok = wait_phase(smem_u32(&ctl->q_full), 0, abort_flag, args.status);
+      tc_fence_after();
+      const uint32_t q_base = smem_u32(s_q);
+      const uint32_t ring_base = smem_u32(s_ring);
+      const int nkv[2] = {nkv0, nkv1};
+
+      auto wait_kv = [&](int t) -> bool {
+        const bool r = wait_phase(smem_u32(&ctl->kv_full[t % G::kSlots]),
+                                  (t / G::kSlots) & 1, abort_flag, args.status);
+        tc_fence_after();
+        return r;
+      };
+      // S_h = Q_h K_j^T into TMEM columns [128h, 128h + 128)
+      auto issue_s = [&](int h, int j) -> bool {
+        const int t = 2 * j;
+        if (!wait_kv(t)) return false;
+        const uint32_t k_tile = ring_base + (t % G::kSlots) * G::kTileBytes;
+        const uint32_t q_tile = q_base + h * G::kTileBytes;
+#pragma unroll
+        for (int kb = 0; kb < G::kKStepsS; ++kb) {
+          const uint32_t off = (kb * G::kKStepBytes / G::kSwBytes) * kTileRows * G::kSwBytes +
+                               (kb * G::kKStepBytes) % G::kSwBytes;
+          const uint64_t da = smem_desc(q_tile + off, 16, 8 * G::kSwBytes, G::kSwMode);
+          const uint64_t db = smem_desc(k_tile + off, 16, 8 * G::kSwBytes, G::kSwMode);
+          if constexpr (FP8)
+            mma_f8_ss(tmem + h * 128, da, db, G::kIdescS, kb > 0);
+          else
+            mma_f16_ss(tmem + h * 128, da, db, G::kIdescS, kb > 0);
+        }
+        tc_commit(smem_u32(&ctl->s_full[h]));
+        const bool last_user = (h == 1) || (j >= nkv[1]);
+        if (last_user) tc_commit(smem_u32(&ctl->kv_empty[t % G::kSlots]));
+        return true;
+      };
+      // O_h += P_h V_j, P_h read from TMEM over S_h's columns
+      auto issue_pv = [&](int h, int j) -> bool {
+        if (!wait_phase(smem_u32(&ctl->p_full[h]), j & 1, abort_flag, args.status)) return false;
+        tc_fence_after();
+        const int t = 2 * j + 1;
+        if (!wait_kv(t)) return false;
+        const uint32_t v_tile = ring_base + (t % G::kSlots) * G::kTileBytes;
+#pragma unroll
+        for (int kb = 0; kb < G::kPvSteps; ++kb) {
+          const uint64_t dv = smem_desc(v_tile + kb * G::kKeysPerPv * G::kSwBytes,
+                                        kTileRows * G::kSwBytes, 8 * G::kSwBytes, G::kSwMode);
+          const uint32_t a = tmem + h * 128 + kb * 8;
+          const uint32_t acc = (j > 0 || kb > 0) ? 1u : 0u;
+          if constexpr (FP8)
+            mma_f8_ts(tmem + 256 + h * 128, a, dv, G::kIdescPV, acc);
+          else
+            mma_f16_ts(tmem + 256 + h * 128, a, dv, G::kIdescPV, acc);
+        }
+        if (j == nkv[h] - 1) tc_commit(smem_u32(&ctl->o_full[h]));
+        const bool last_user = (h == 1) || (j >= nkv[1]);
+        if (last_user) tc_commit(smem_u32(&ctl->kv_empty[t % G::kSlots]));
+        return true;
+      };
+
+      if (ok && nkv0 > 0) ok = issue_s(0, 0);
+      if (ok && nkv1 > 0) ok = issue_s(1, 0);
+      for (int j = 0; j < nkv_load && ok; ++j) {
+#pragma unroll
+        for (int h = 0; h < 2 && ok; ++h) {
+          if (j < nkv[h]) {
+            ok = issue_pv(h, j);
+            if (ok && j + 1 < nkv[h]) ok = issue_s(h, j + 1);
+          }
+        }
+      }
+      // make sure nothing this thread issued is still running before TMEM is released
+      tc_commit(smem_u32(&ctl->drain));
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(smem_u32(&ctl->drain), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+  }
+  } else {
+    regs_inc<216>();
+    // ============================================================ softmax / epilogue
+    const int h = warp / 4;
+    const int w4 = warp % 4;
+    const int nkv_h = h == 0 ? nkv0 : nkv1;
+    const int r_local = w4 * 32 + lane;        // TMEM lane == row within the tile
+    const int row = row0 + h * kTileRows + r_local;
+    const uint32_t lane_addr = static_cast<uint32_t>(w4 * 32) << 16;
+    const uint32_t t_s = tmem + lane_addr + h * 128;        // S_h / P_h
+    const uint32_t t_o = tmem + lane_addr + 256 + h * 128;  // O_h
+    const float c = args.c;
+    float m_run = -INFINITY;  // running max of scaled logits, log2 units
+    float l_run = 0.f;        // running sum of 2^(x - m_run)
+    bool ok = true;
+
+    for (int j = 0; j < nkv_h; ++j) {
+      ok = wait_phase(smem_u32(&ctl->s_full[h]), j & 1, abort_flag, args.status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+
+      float s[128];
+      {
+        uint32_t r[32];
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) {
+          tmem_ld32(t_s + cb * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[cb * 32 + i] = __uint_as_float(r[i]);
+        }
+      }
+      // masks: keys past the end of the sequence, and the causal diagonal block
+      const int key0 = j * kTileRows;
+      const bool masked = (key0 + kTileRows > n) || (CAUSAL && j == nkv_h - 1);
+      int lim = kTileRows;  // keys < lim are visible to this row
+      if (masked) {
+        const int lim_c = (CAUSAL && j == nkv_h - 1) ? r_local + 1 : kTileRows;
+        lim = min(n - key0, lim_c);
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i >= lim) s[i] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
+      const float m_new = fmaxf(m_run, mx * c);
+      const float alpha = ex2_mufu(m_run - m_new);  // 0 on the first block (m_run = -inf)
+
+      // rescale O_h by alpha when the running max moved (warp-uniform: tcgen05 is collective)
+      if (j > 0 && __any_sync(0xffffffffu, m_new > m_run)) {
+        uint32_t r[32];
+#pragma unroll
+        for (int cb = 0; cb < D / 32; ++cb) {
+          tmem_ld32(t_o + cb * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          tmem_st32(t_o + cb * 32, r);
+        }
+      }
+      m_run = m_new;
+
+      // probabilities p = 2^(s c - m); masked keys get exactly 0
+      float rowsum = 0.f;
+      if (masked) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+          s[i] = i < lim ? ex2_mufu(fmaf(s[i], c, -m_new)) : 0.f;
+          rowsum += s[i];
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+          s[i] = ex2_mufu(fmaf(s[i], c, -m_new));
+          rowsum += s[i];
+        }
+      }
+      l_run = l_run * alpha + rowsum;
+
+      // write P over S_h (packed), then signal the MMA warp
+      if constexpr (FP8) {
+        uint32_t r[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          r[i] = pack_e4m3x4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]);
+        tmem_st32(t_s, r);
+      } else {
+        uint32_t r[32];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            r[i] = pack_bf16x2(s[64 * half + 2 * i], s[64 * half + 2 * i + 1]);
+          tmem_st32(t_s + 32 * half, r);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full[h]));
+    }
+
+    if (ok && nkv_h > 0) {
+      ok = wait_phase(smem_u32(&ctl->o_full[h]), 0, abort_flag, args.status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = args.out_mult / l_run;
+        const bool live = row < n;
+        __nv_bfloat16* orow = args.o + (static_cast<size_t>(bh) * n + (live ? row : 0)) * D;
+#pragma unroll
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t r[32];
+          tmem_ld32(t_o + cb * 32, r);
+          tmem_ld_wait();
+          uint32_t packed[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            packed[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l,
+                                    __uint_as_float(r[2 * i + 1]) * inv_l);
+          if (live) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + cb * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                  packed[4 * i + 3]);
+          }
+        }
+        if (live)
+          args.lse[static_cast<size_t>(bh) * n + row] = (m_run + lg2_mufu(l_run)) * kLn2;
+      }
+    }
+    tc_fence_before();
+  }
+
+  // ---------------------------------------------------------------- teardown
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+
+}  // namespace exattn

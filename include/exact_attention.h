@@ -1,0 +1,121 @@
+/*
+ * exact_attention.h -- C ABI of libexattn.so, the fused exact-attention forward for sm_103a.
+ *
+ * The operation (problem statement of "FlashAttention · InkStack", opening of "FlashAttention 1:
+ * Data Movement", and the stored statistic of its section 2.1 "优化 Online Softmax"):
+ *
+ *     O   = softmax(scale * Q K^T + mask) V
+ *     LSE = log sum_j exp(scale * q_i . k_j)     (natural log, over the keys row i may see)
+ *
+ * computed in one kernel launch without writing the N x N scores or probabilities anywhere:
+ * Q is tiled into 128-row blocks, K/V are streamed in 128-row blocks, and each row keeps the
+ * online-softmax state (running max m, running sum l, unnormalised output) on chip, merged with
+ * the rescale factor alpha = e^(m_old - m_new) ("FlashAttention · InkStack", section 1.1.2).
+ * The causal mask is lower-triangular with the diagonal included (key j visible to query i iff
+ * j <= i); fully masked key blocks are skipped.
+ *
+ * Layout (all row-major, head dimension fastest, no padding between rows):
+ *   q, k, v : [B, H, N, d], bf16 or fp8 e4m3fn (all three the same dtype)
+ *   o       : [B, H, N, d], bf16 for both operand dtypes
+ *   lse     : [B, H, N], fp32
+ *
+ * Ownership: every pointer is caller-owned device memory.  The library allocates no device
+ * memory, frees nothing and keeps no pointer after the call returns.  The kernel runs
+ * asynchronously on `stream` (a cudaStream_t, NULL = legacy default stream); the caller keeps
+ * the buffers alive until the stream has passed the launch.  No call synchronises the stream.
+ *
+ * Errors: arguments are checked on the host before anything is launched; a failed check returns
+ * a status code and launches nothing.  A launch failure returns FA_ERR_CUDA.  Inside the kernel
+ * every wait is bounded in time; a wait that runs out makes the kernel stop early, free its
+ * tensor memory and record FA_ERR_DEVICE_TIMEOUT in the device status word (see
+ * fa_device_status / fa_fwd_opts.dev_status).  No exception crosses this interface.
+ */
+#ifndef EXACT_ATTENTION_H
+#define EXACT_ATTENTION_H
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_DTYPE_BF16 = 0,     /* q, k, v are bf16 */
+  FA_DTYPE_FP8_E4M3 = 1  /* q, k, v are fp8 e4m3fn with per-tensor fp32 descales */
+} fa_dtype;
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,    /* null pointer, non-positive size, bad scale or dtype */
+  FA_ERR_UNSUPPORTED = 2,    /* head dim not in {64, 128}, or sizes beyond the kernel's limits */
+  FA_ERR_MISALIGNED = 3,     /* a pointer is not 16-byte aligned */
+  FA_ERR_CUDA = 4,           /* a CUDA runtime or driver call failed (no device, launch error) */
+  FA_ERR_DEVICE_TIMEOUT = 5  /* a bounded wait inside the kernel ran out; outputs are invalid */
+} fa_status;
+
+/*
+ * Attention forward.
+ *   q, k, v : device pointers, [B, H, N, d] of `dtype` (16-byte aligned)
+ *   o       : device pointer, [B, H, N, d] bf16 (16-byte aligned)
+ *   lse     : device pointer, [B, H, N] fp32 (4-byte aligned)
+ *   B, H, N : >= 1, with B * H <= 65535 and N < 2^31 - 256
+ *   d       : head dimension, 64 or 128
+ *   scale   : softmax scale applied to q . k, finite and >= 0 (usually 1/sqrt(d))
+ *   causal  : 0 = no mask, nonzero = lower-triangular mask (diagonal included)
+ *   dtype   : an fa_dtype; FP8_E4M3 uses descales of 1.0 here (see fa_fwd_ex)
+ *   stream  : a cudaStream_t
+ * Returns an fa_status.
+ */
+FA_API int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+           int d, float scale, int causal, int dtype, void* stream);
+
+/*
+ * Options of fa_fwd_ex.  For fp8 operands the stored values are code * descale: the scores are
+ * scale * descale_q * descale_k * (q . k) and the output is descale_v * (P V) (per-tensor
+ * scaling of "FlashAttention · InkStack", section 3.3.3 "Scaling").  The descales must be
+ * finite and > 0; they are ignored for bf16.  `dev_status`, if not NULL, is a device int the
+ * kernel sets to FA_ERR_DEVICE_TIMEOUT when a wait runs out (it never writes FA_OK: clear it
+ * before the call); if NULL the library's own per-device status word is used instead.
+ */
+typedef struct {
+  float descale_q;
+  float descale_k;
+  float descale_v;
+  int* dev_status;
+} fa_fwd_opts;
+
+/* fa_fwd with options; `opts` may be NULL (descales 1.0, library status word). */
+FA_API int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+              int N, int d, float scale, int causal, int dtype, const fa_fwd_opts* opts,
+              void* stream);
+
+/*
+ * Read, and if `clear` is nonzero reset to FA_OK, the library's status word on the current
+ * device.  Synchronises the device first.  Writes FA_OK or FA_ERR_DEVICE_TIMEOUT to *out.
+ * Returns an fa_status for the call itself.
+ */
+FA_API int fa_device_status(int clear, int* out);
+
+/* A static, human-readable name for a status code. */
+FA_API const char* fa_status_string(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+FA_API int fa_version(void);
+
+/*
+ * Diagnostic: evaluate the kernel's own 2^x routines on n inputs, for testing them against
+ * exact exp2.  mode 0 = hardware approximation (MUFU ex2), mode 1 = the FMA polynomial
+ * emulation the softmax uses for part of its columns ("FlashAttention4 精读", section 3.1.3
+ * "Emulation of the exponential function").  x, y are device float arrays of n elements.
+ */
+FA_API int fa_debug_exp2(const float* x, float* y, long long n, int mode, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_ATTENTION_H */

@@ -1,0 +1,213 @@
+"""GPU parity: the CUDA kernel (through the C ABI) against the fp64 oracle on the same bytes."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle
+from tests.parity import compare
+from workloads import WORKLOADS, make_inputs, random_inputs, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def ea():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import exact_attention_13_gb300 as mod
+
+    mod.lib()
+    mod.device_status(clear=True)
+    yield mod
+    assert mod.device_status(clear=True) == 0
+
+
+def run(ea, inp, causal, scale=None):
+    q, k, v = (getattr(inp, n).to(DEV) for n in "qkv")
+    o, lse = ea.fwd(q, k, v, causal=causal, scale=scale,
+                    descale=(inp.descale_q, inp.descale_k, inp.descale_v))
+    torch.cuda.synchronize()
+    return o, lse
+
+
+SMALL = [
+    # (B, H, N, d, dtype, causal)
+    (1, 1, 1, 64, "bf16", False),
+    (1, 1, 1, 128, "bf16", True),
+    (1, 2, 100, 128, "bf16", False),
+    (1, 2, 128, 128, "bf16", True),
+    (1, 1, 129, 64, "bf16", True),
+    (2, 2, 256, 128, "bf16", False),
+    (1, 3, 300, 64, "bf16", False),
+    (1, 3, 300, 128, "bf16", True),
+    (1, 1, 513, 128, "bf16", True),
+    (2, 1, 640, 64, "bf16", True),
+    (1, 2, 1000, 128, "bf16", False),
+    (1, 1, 1, 128, "e4m3", False),
+    (1, 2, 200, 128, "e4m3", False),
+    (1, 2, 300, 128, "e4m3", True),
+    (1, 2, 257, 64, "e4m3", False),
+    (1, 1, 700, 64, "e4m3", True),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,dtype,causal", SMALL,
+                         ids=[f"B{b}H{h}N{n}d{d}-{t}-{'causal' if c else 'full'}"
+                              for b, h, n, d, t, c in SMALL])
+def test_small_full_parity(ea, B, H, N, d, dtype, causal):
+    inp = random_inputs(B, H, N, d, dtype, seed=N * 7 + d + B * 3 + H + int(causal))
+    o, lse = run(ea, inp, causal)
+    o_ref, l_ref = oracle.attention_fwd_inputs(inp, 1.0 / math.sqrt(d), causal)
+    compare(o, lse, o_ref, l_ref, dtype, f"{(B, H, N, d, dtype, causal)}")
+
+
+@pytest.mark.parametrize("name", ["b1h1n256d64_bf16", "b4h16n2048d128_bf16_causal",
+                                  "b4h16n2048d128_bf16_causal_q8"])
+def test_workload_full_parity(ea, name):
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    o, lse = run(ea, inp, w.causal)
+    o_ref, l_ref = oracle.attention_fwd_inputs(inp, w.scale, w.causal)
+    stats = compare(o, lse, o_ref, l_ref, w.dtype, name)
+    print(name, stats)
+
+
+@pytest.mark.parametrize("name", ["b2h32n8192d128_bf16", "b1h16n32768d64_bf16_causal",
+                                  "b2h32n16384d128_e4m3"])
+def test_workload_sampled_parity(ea, name):
+    """Full-size launch; the oracle checks a sample of rows of every head one by one."""
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    o, lse = run(ea, inp, w.causal)
+    rows = sample_rows(w.N, w.seed)
+    o_ref, l_ref = oracle.attention_fwd_inputs(inp, w.scale, w.causal, rows=rows)
+    stats = compare(o[:, :, rows], lse[:, :, rows], o_ref, l_ref, w.dtype, name)
+    print(name, stats)
+    # properties that hold for every row: finite, LSE >= max logit's lower bound log(1)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+
+
+def test_identical_keys_give_mean_of_values(ea):
+    B, H, N, d = 1, 2, 300, 128
+    inp = random_inputs(B, H, N, d, "bf16", seed=91)
+    inp.k[:] = inp.k[:, :, :1, :]
+    for causal in (False, True):
+        o, lse = run(ea, inp, causal)
+        o_ref, l_ref = oracle.attention_fwd_inputs(inp, 1 / math.sqrt(d), causal)
+        v = inp.v.double().numpy()
+        if causal:
+            want = np.cumsum(v, axis=2) / np.arange(1, N + 1)[None, None, :, None]
+        else:
+            want = np.broadcast_to(v.mean(axis=2, keepdims=True), v.shape)
+        np.testing.assert_allclose(o_ref, want, atol=1e-12)
+        compare(o, lse, o_ref, l_ref, "bf16", f"identical keys causal={causal}")
+
+
+def test_dominant_logit_selects_value_row(ea):
+    B, H, N, d = 1, 1, 384, 64
+    inp = random_inputs(B, H, N, d, "bf16", seed=92)
+    J = 200
+    # key J aligned with every query's direction is not possible for all rows; make key J
+    # huge along q_i for a chosen row i and check that row
+    i = 333
+    qi = inp.q[0, 0, i].double()
+    kJ = (80.0 * math.sqrt(d)) * qi / qi.dot(qi)
+    inp.k[0, 0, J] = kJ.to(torch.bfloat16)
+    o, lse = run(ea, inp, False)
+    o_ref, l_ref = oracle.attention_fwd_inputs(inp, 1 / math.sqrt(d), False)
+    compare(o, lse, o_ref, l_ref, "bf16", "dominant logit")
+    np.testing.assert_allclose(o[0, 0, i].double().cpu().numpy(), inp.v[0, 0, J].double().numpy(),
+                               atol=1e-2)
+
+
+def test_causal_row_zero_is_v0_exactly(ea):
+    inp = random_inputs(2, 3, 260, 128, "bf16", seed=93)
+    o, lse = run(ea, inp, True)
+    torch.testing.assert_close(o[:, :, 0].cpu(), inp.v[:, :, 0], rtol=0, atol=0)
+    x00 = (inp.q[:, :, 0].double() * inp.k[:, :, 0].double()).sum(-1) / math.sqrt(128)
+    torch.testing.assert_close(lse[:, :, 0].double().cpu(), x00, rtol=0, atol=1e-4)
+
+
+def test_no_writes_past_the_outputs(ea):
+    B, H, N, d = 1, 2, 300, 128
+    inp = random_inputs(B, H, N, d, "bf16", seed=94)
+    q, k, v = (getattr(inp, n).to(DEV) for n in "qkv")
+    n_o = B * H * N * d
+    o_buf = torch.full((n_o + 4096,), 7.0, dtype=torch.bfloat16, device=DEV)
+    l_buf = torch.full((B * H * N + 1024,), 7.0, dtype=torch.float32, device=DEV)
+    o = o_buf[:n_o].view(B, H, N, d)
+    lse = l_buf[: B * H * N].view(B, H, N)
+    for causal in (False, True):
+        ea.fwd(q, k, v, causal=causal, out=o, lse=lse)
+        torch.cuda.synchronize()
+        assert (o_buf[n_o:] == 7.0).all()
+        assert (l_buf[B * H * N:] == 7.0).all()
+
+
+def test_fp8_with_unit_descales(ea):
+    """e4m3 codes used as plain values (descale 1): the kernel must not assume amax scaling."""
+    B, H, N, d = 1, 2, 300, 128
+    g = torch.Generator().manual_seed(95)
+    vals = (torch.randn((3, B, H, N, d), generator=g) * 0.5).to(torch.float8_e4m3fn)
+    from workloads import Inputs
+
+    inp = Inputs(vals[0], vals[1], vals[2])
+    for causal in (False, True):
+        o, lse = run(ea, inp, causal, scale=0.3)
+        o_ref, l_ref = oracle.attention_fwd_inputs(inp, 0.3, causal)
+        compare(o, lse, o_ref, l_ref, "e4m3", f"fp8 unit descale causal={causal}")
+
+
+def test_scale_zero_gives_uniform_weights(ea):
+    inp = random_inputs(1, 1, 200, 64, "bf16", seed=96)
+    o, lse = run(ea, inp, False, scale=0.0)
+    o_ref, l_ref = oracle.attention_fwd_inputs(inp, 0.0, False)
+    compare(o, lse, o_ref, l_ref, "bf16", "scale 0")
+
+
+def test_repeat_calls_are_deterministic(ea):
+    inp = random_inputs(1, 4, 1000, 128, "bf16", seed=97)
+    o1, l1 = run(ea, inp, True)
+    o2, l2 = run(ea, inp, True)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_host_validation_launches_nothing(ea):
+    x = torch.zeros((1, 1, 128, 128), dtype=torch.bfloat16, device=DEV)
+    lse = torch.zeros((1, 1, 128), dtype=torch.float32, device=DEV)
+    p = x.data_ptr()
+    s = torch.cuda.current_stream().cuda_stream
+    assert ea.fa_fwd(p, p, p, p, lse.data_ptr(), 1, 1, 128, 96, 0.1, 0, 0, s) == ea.FA_ERR_UNSUPPORTED
+    assert ea.fa_fwd(p + 2, p, p, p, lse.data_ptr(), 1, 1, 128, 128, 0.1, 0, 0, s) == ea.FA_ERR_MISALIGNED
+    assert ea.fa_fwd(p, p, p, p, lse.data_ptr(), 1, 1, 0, 128, 0.1, 0, 0, s) == ea.FA_ERR_INVALID_ARG
+    assert ea.fa_fwd(p, p, p, p, lse.data_ptr(), 1, 1, 128, 128, -1.0, 0, 0, s) == ea.FA_ERR_INVALID_ARG
+    assert ea.fa_fwd(p, p, p, p, lse.data_ptr(), 1, 1, 128, 128, float("nan"), 0, 0, s) == ea.FA_ERR_INVALID_ARG
+    assert ea.fa_fwd(p, p, p, p, lse.data_ptr(), 1, 1, 128, 128, 0.1, 0, 7, s) == ea.FA_ERR_INVALID_ARG
+    assert ea.fa_fwd_ex(p, p, p, p, lse.data_ptr(), 1, 1, 128, 128, 0.1, 0, 1, (1.0, 0.0, 1.0),
+                        None, s) == ea.FA_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+
+
+def test_exp2_routines(ea):
+    """MUFU ex2 and the FMA-polynomial 2^x against exact exp2 on [-126, 0]: the polynomial's
+    maximum relative error stays within the degree-3 figure of "FlashAttention4 精读" section
+    3.1.3 (8.77e-5), and for 99% of inputs it agrees with MUFU within one bf16 ulp."""
+    x = torch.linspace(-126.0, 0.0, 1 << 22, dtype=torch.float32, device=DEV)
+    x = torch.cat([x, torch.rand(1 << 20, device=DEV, dtype=torch.float32) * -20.0])
+    want = torch.exp2(x.double())
+    y0 = ea.debug_exp2(x, 0).double()
+    y1 = ea.debug_exp2(x, 1).double()
+    rel0 = ((y0 - want).abs() / want).max().item()
+    rel1 = ((y1 - want).abs() / want).max().item()
+    assert rel0 < 2e-6, rel0
+    assert rel1 < 8.77e-5, rel1
+    b0 = y0.to(torch.bfloat16)
+    b1 = y1.to(torch.bfloat16)
+    ulp = (b0.view(torch.int16).int() - b1.view(torch.int16).int()).abs()
+    assert (ulp <= 1).float().mean().item() >= 0.99
