@@ -64,7 +64,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except (OSError, FileNotFoundError):
@@ -104,35 +104,46 @@ class ClockSampler:
                 "power_w_max": pmax, "samples": len(loaded), "reasons": reasons}
 
 
-def oracle_sample_rate(inp, w, target_s: float, seed: int = 0):
-    """Time the fp64 oracle on a sample of rows sized for about target_s; return TFLOPS-equiv."""
+def oracle_sample_rate(inp, w, target_s: float):
+    """Time the fp64 oracle on a sample of the workload sized for about target_s seconds.
+
+    The sample is a set of query rows (spread over the sequence) of the first heads; the rate is
+    the attention-forward flops of those rows (4 * keys * d each) per second, in TFLOPS.
+    """
     from oracle import oracle
 
     orc = oracle.get()
     cores = os.cpu_count() or 1
-    heads = min(w.B * w.H, 4)
-    sub = type(inp)(inp.q[:1, :heads], inp.k[:1, :heads], inp.v[:1, :heads],
-                    inp.descale_q, inp.descale_k, inp.descale_v) if w.B * w.H > 1 else inp
-    rng_rows = list(range(w.N - 1, -1, -max(1, w.N // 4096)))  # spread over the sequence
+    bh = w.B * w.H
+    stride = max(1, w.N // 4096)
+    rows_all = list(range(w.N - 1, -1, -stride))
 
-    def run(nrows):
-        rows = sorted(rng_rows[:nrows])
+    def run(heads, nrows):
+        b_heads = min(heads, w.H)
+        nb = (heads + w.H - 1) // w.H
+        sub = type(inp)(inp.q[:nb, :b_heads], inp.k[:nb, :b_heads], inp.v[:nb, :b_heads],
+                        inp.descale_q, inp.descale_k, inp.descale_v)
+        rows = sorted(rows_all[:nrows])
         t0 = time.perf_counter()
         orc.attention_fwd(sub.raw("q"), sub.raw("k"), sub.raw("v"), w.scale, w.causal, sub.dtype,
                           (sub.descale_q, sub.descale_k, sub.descale_v), rows, cores)
         dt = time.perf_counter() - t0
         keys = sum((r + 1) if w.causal else w.N for r in rows)
-        flops = 4.0 * keys * w.d * sub.q.shape[1]
-        return flops, dt, len(rows)
+        nh = sub.q.shape[0] * sub.q.shape[1]
+        return 4.0 * keys * w.d * nh / dt / 1e12, dt, nh, len(rows)
 
-    n = min(len(rng_rows), 64)
-    flops, dt, nr = run(n)
-    if dt < target_s:
-        n = min(len(rng_rows), max(n, int(n * target_s / max(dt, 1e-3))))
-        flops, dt, nr = run(n)
-    sample = (f"{nr} query rows x {sub.q.shape[1]} heads of {w.name} "
-              f"({'causal' if w.causal else 'all'} keys each), fp64")
-    return flops / dt / 1e12, dt, cores, sample
+    heads, nrows = min(bh, 2), min(len(rows_all), 256)
+    tf, dt, nh, nr = run(heads, nrows)
+    # grow rows first, then heads, to reach the target duration
+    scale = target_s / max(dt, 1e-3)
+    if scale > 1.2:
+        nrows = min(len(rows_all), int(nrows * scale))
+        scale /= nrows / max(nr, 1)
+        heads = min(bh, max(heads, int(heads * max(scale, 1.0))))
+        tf, dt, nh, nr = run(heads, nrows)
+    sample = (f"{nr} query rows x {nh} heads of {w.name} "
+              f"({'causal' if w.causal else 'all'} keys each), fp64 on {cores} threads")
+    return tf, dt, cores, sample
 
 
 KERNEL_SOURCES = ["exact_attention_13_gb300/csrc/fa_fwd_kernel.cuh",
@@ -340,7 +351,7 @@ def run_ours(args, w, world, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

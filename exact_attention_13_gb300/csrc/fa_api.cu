@@ -203,6 +203,16 @@ const char* fa_status_string(int status) {
 
 int fa_version(void) { return 100; }
 
+#ifdef EXATTN_TRACE
+// Diagnostic builds only: point the timeline trace at a device buffer of
+// 10 * 2 * kTraceMaxJ int64 and pick the CTA (blockIdx.x + gridDim.x * blockIdx.y) to record.
+FA_API int fa_trace_config(long long* buf, int cta) {
+  if (cudaMemcpyToSymbol(g_trace_buf, &buf, sizeof(buf)) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaMemcpyToSymbol(g_trace_cta, &cta, sizeof(cta)) != cudaSuccess) return FA_ERR_CUDA;
+  return FA_OK;
+}
+#endif
+
 int fa_debug_exp2(const float* x, float* y, long long n, int mode, void* stream) {
   if (!x || !y || n < 0 || (mode != 0 && mode != 1)) return FA_ERR_INVALID_ARG;
   if (n == 0) return FA_OK;

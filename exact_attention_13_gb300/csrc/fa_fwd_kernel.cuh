@@ -41,12 +41,44 @@
 
 namespace exattn {
 
+// Optional timeline trace (build with -DEXATTN_TRACE): one CTA records clock64() at the role
+// hand-offs into a device buffer of 10 x 2 x kTraceMaxJ int64, for profiling the pipeline.
+// Compiled out by default.
+#ifdef EXATTN_TRACE
+__device__ long long* g_trace_buf;
+__device__ int g_trace_cta;
+constexpr int kTraceMaxJ = 512;
+#define EXATTN_TRACE_SETUP                                                                 \
+  long long* const trace_buf =                                                             \
+      ((int)(blockIdx.x + gridDim.x * blockIdx.y) == g_trace_cta) ? g_trace_buf : nullptr
+#define EXATTN_TRACE_EVENT(kind, h, j)                                                     \
+  do {                                                                                     \
+    if (trace_buf && (j) < kTraceMaxJ) trace_buf[((kind) * 2 + (h)) * kTraceMaxJ + (j)] = clock64(); \
+  } while (0)
+#else
+#define EXATTN_TRACE_SETUP \
+  do {                     \
+  } while (0)
+#define EXATTN_TRACE_EVENT(kind, h, j) \
+  do {                                 \
+  } while (0)
+#endif
+
 constexpr int kThreads = 384;
 constexpr int kTileRows = 128;       // query rows per Q tile, keys per K/V block
 constexpr int kCtaRows = 2 * kTileRows;
 constexpr int kStatusTimeout = 5;    // FA_ERR_DEVICE_TIMEOUT
 constexpr uint64_t kWaitLimitNs = 4ull * 1000 * 1000 * 1000;  // 4 s per wait
 constexpr float kLn2 = 0.6931471805599453f;
+// Rescale threshold (log2 units).  0 rescales whenever a row's max grows; a positive value is the
+// lazy rescale of "FlashAttention4 精读", section 3.1.4 (the page uses 8, a factor 2^8), which
+// keeps a stale max and lets probabilities reach 2^threshold.  Exact in real arithmetic, but P
+// values above 1 are not exact in bf16/e4m3, so the dominant probability of a peaked row picks
+// up a rounding error (2^-9 relative in bf16) that the threshold-0 schedule avoids (there the
+// row max maps to exactly 1).  On logits spread over +-100 that costs up to ~0.009 in O, enough
+// to cross the 1e-2 gate, so the kernel uses 0.
+constexpr float kRescaleLog2 = 0.0f;
+constexpr int kL2PrefetchBlocks = 6;  // K/V blocks warmed in L2 ahead of the ring
 
 struct KernelArgs {
   __nv_bfloat16* o;   // [BH, N, d]
@@ -66,7 +98,7 @@ struct Geo {
   static constexpr int kBoxes = kRowBytes / kSwBytes;       // TMA boxes per 128-row tile
   static constexpr int kBoxElems = kSwBytes / kElem;        // inner box extent (elements)
   static constexpr int kTileBytes = kTileRows * kRowBytes;  // one 128-row operand tile
-  static constexpr int kSlots = (FP8 || D == 64) ? 8 : 4;   // K/V ring depth
+  static constexpr int kSlots = (FP8 || D == 64) ? 8 : 5;   // K/V ring depth
   static constexpr int kQBytes = 2 * kTileBytes;
   static constexpr int kRingBytes = kSlots * kTileBytes;
   static constexpr uint32_t kSwMode = kSwBytes == 128 ? kSwizzle128B : kSwizzle64B;
@@ -86,7 +118,7 @@ struct Ctrl {
   uint64_t kv_full[kSlots];
   uint64_t kv_empty[kSlots];
   uint64_t s_full[2];
-  uint64_t p_full[2];
+  uint64_t p_full[2][2];  // [tile][half of the keys]
   uint64_t o_full[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -142,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int n = args.n;
+  EXATTN_TRACE_SETUP;
   const int bh = blockIdx.y;
   // heaviest query blocks first under the causal mask (they see the most keys)
   const int mblock = CAUSAL ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x;
@@ -163,7 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(smem_u32(&ctl->s_full[h]), 1);
-      mbar_init(smem_u32(&ctl->p_full[h]), 4);  // one arrival per softmax warp
+      mbar_init(smem_u32(&ctl->p_full[h][0]), 4);  // one arrival per softmax warp
+      mbar_init(smem_u32(&ctl->p_full[h][1]), 4);
       mbar_init(smem_u32(&ctl->o_full[h]), 1);
     }
     mbar_init(smem_u32(&ctl->drain), 1);
@@ -199,6 +233,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                              &map_q, qbar, b * G::kBoxElems, row0 + h * kTileRows, bh, once);
         }
       }
+      // L2 warm-up of the first K/V blocks; the loop keeps it kL2PrefetchBlocks ahead
+      for (int j = 0; j < kL2PrefetchBlocks && j < nkv_load; ++j)
+        for (int b = 0; b < G::kBoxes; ++b) {
+          tma_prefetch_l2_3d(&map_k, b * G::kBoxElems, j * kTileRows, bh);
+          tma_prefetch_l2_3d(&map_v, b * G::kBoxElems, j * kTileRows, bh);
+        }
       int issued = 0;
       bool ok = true;
       for (int t = 0; t < 2 * nkv_load && ok; ++t) {
@@ -210,12 +250,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
         const uint32_t fbar = smem_u32(&ctl->kv_full[slot]);
+        EXATTN_TRACE_EVENT(9, t & 1, t >> 1);
         mbar_arrive_expect_tx(fbar, G::kTileBytes);
         const CUtensorMap* map = (t & 1) ? &map_v : &map_k;
         uint8_t* dst = s_ring + slot * G::kTileBytes;
         for (int b = 0; b < G::kBoxes; ++b)
           tma_load_3d_hint(smem_u32(dst + b * kTileRows * G::kSwBytes), map, fbar,
                            b * G::kBoxElems, (t >> 1) * kTileRows, bh, keep);
+        const int jp = (t >> 1) + kL2PrefetchBlocks;
+        if (jp < nkv_load)
+          for (int b = 0; b < G::kBoxes; ++b)
+            tma_prefetch_l2_3d(map, b * G::kBoxElems, jp * kTileRows, bh);
         ++issued;
       }
       if (!ok) {
@@ -250,6 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_s = [&](int h, int j) -> bool {
         const int t = 2 * j;
         if (!wait_kv(t)) return false;
+        EXATTN_TRACE_EVENT(7, h, j);
         const uint32_t k_tile = ring_base + (t % G::kSlots) * G::kTileBytes;
         const uint32_t q_tile = q_base + h * G::kTileBytes;
 #pragma unroll
@@ -264,28 +310,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_f16_ss(tmem + h * 128, da, db, G::kIdescS, kb > 0);
         }
         tc_commit(smem_u32(&ctl->s_full[h]));
+        EXATTN_TRACE_EVENT(6, h, j);
         const bool last_user = (h == 1) || (j >= nkv[1]);
         if (last_user) tc_commit(smem_u32(&ctl->kv_empty[t % G::kSlots]));
         return true;
       };
-      // O_h += P_h V_j, P_h read from TMEM over S_h's columns
+      // O_h += P_h V_j, P_h read from TMEM over S_h's columns.  The softmax publishes P in two
+      // halves of 64 keys; the MMAs of the first half start while the second is computed.
       auto issue_pv = [&](int h, int j) -> bool {
-        if (!wait_phase(smem_u32(&ctl->p_full[h]), j & 1, abort_flag, args.status)) return false;
-        tc_fence_after();
         const int t = 2 * j + 1;
         if (!wait_kv(t)) return false;
+        EXATTN_TRACE_EVENT(8, h, j);
         const uint32_t v_tile = ring_base + (t % G::kSlots) * G::kTileBytes;
 #pragma unroll
-        for (int kb = 0; kb < G::kPvSteps; ++kb) {
-          const uint64_t dv = smem_desc(v_tile + kb * G::kKeysPerPv * G::kSwBytes,
-                                        kTileRows * G::kSwBytes, 8 * G::kSwBytes, G::kSwMode);
-          const uint32_t a = tmem + h * 128 + kb * 8;
-          const uint32_t acc = (j > 0 || kb > 0) ? 1u : 0u;
-          if constexpr (FP8)
-            mma_f8_ts(tmem + 256 + h * 128, a, dv, G::kIdescPV, acc);
-          else
-            mma_f16_ts(tmem + 256 + h * 128, a, dv, G::kIdescPV, acc);
+        for (int half = 0; half < 2; ++half) {
+          if (!wait_phase(smem_u32(&ctl->p_full[h][half]), j & 1, abort_flag, args.status))
+            return false;
+          tc_fence_after();
+          if (half == 0) EXATTN_TRACE_EVENT(4, h, j);
+#pragma unroll
+          for (int kk = 0; kk < G::kPvSteps / 2; ++kk) {
+            const int kb = half * (G::kPvSteps / 2) + kk;
+            const uint64_t dv = smem_desc(v_tile + kb * G::kKeysPerPv * G::kSwBytes,
+                                          kTileRows * G::kSwBytes, 8 * G::kSwBytes, G::kSwMode);
+            const uint32_t a = tmem + h * 128 + kb * 8;
+            const uint32_t acc = (j > 0 || kb > 0) ? 1u : 0u;
+            if constexpr (FP8)
+              mma_f8_ts(tmem + 256 + h * 128, a, dv, G::kIdescPV, acc);
+            else
+              mma_f16_ts(tmem + 256 + h * 128, a, dv, G::kIdescPV, acc);
+          }
         }
+        EXATTN_TRACE_EVENT(5, h, j);
         if (j == nkv[h] - 1) tc_commit(smem_u32(&ctl->o_full[h]));
         const bool last_user = (h == 1) || (j >= nkv[1]);
         if (last_user) tc_commit(smem_u32(&ctl->kv_empty[t % G::kSlots]));
@@ -331,17 +387,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
+      if (threadIdx.x % 128 == 0) EXATTN_TRACE_EVENT(0, h, j);
 
+      // the row of S: four TMEM loads in flight, one wait
       float s[128];
       {
-        uint32_t r[32];
+        uint32_t r[4][32];
 #pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
-          tmem_ld32(t_s + cb * 32, r);
-          tmem_ld_wait();
+        for (int cb = 0; cb < 4; ++cb) tmem_ld32(t_s + cb * 32, r[cb]);
+        tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) s[cb * 32 + i] = __uint_as_float(r[i]);
-        }
+        for (int cb = 0; cb < 4; ++cb)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[cb * 32 + i] = __uint_as_float(r[cb][i]);
       }
       // masks: keys past the end of the sequence, and the causal diagonal block
       const int key0 = j * kTileRows;
@@ -354,14 +412,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 128; ++i)
           if (i >= lim) s[i] = -INFINITY;
       }
-      float mx = s[0];
+      // row max: eight independent partial maxima, then a tree
+      float mp[8];
 #pragma unroll
-      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
-      const float m_new = fmaxf(m_run, mx * c);
-      const float alpha = ex2_mufu(m_run - m_new);  // 0 on the first block (m_run = -inf)
+      for (int k = 0; k < 8; ++k) mp[k] = s[k];
+#pragma unroll
+      for (int i = 8; i < 128; ++i) mp[i % 8] = fmaxf(mp[i % 8], s[i]);
+#pragma unroll
+      for (int w = 4; w >= 1; w /= 2)
+#pragma unroll
+        for (int k = 0; k < w; ++k) mp[k] = fmaxf(mp[k], mp[k + w]);
+      const float m_cand = fmaxf(m_run, mp[0] * c);
+      if (threadIdx.x % 128 == 0) EXATTN_TRACE_EVENT(1, h, j);
 
-      // rescale O_h by alpha when the running max moved (warp-uniform: tcgen05 is collective)
-      if (j > 0 && __any_sync(0xffffffffu, m_new > m_run)) {
+      // Rescale O and l when some row of the warp grew its max by more than kRescaleLog2 (the
+      // decision is warp-uniform because tcgen05.ld/st are warp-collective; rows whose max did
+      // not move get alpha = 1).
+      if (j == 0) {
+        m_run = m_cand;
+      } else if (__any_sync(0xffffffffu, m_cand - m_run > kRescaleLog2)) {
+        const float alpha = ex2_mufu(m_run - m_cand);
         uint32_t r[32];
 #pragma unroll
         for (int cb = 0; cb < D / 32; ++cb) {
@@ -371,47 +441,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
           tmem_st32(t_o + cb * 32, r);
         }
+        l_run *= alpha;
+        m_run = m_cand;
       }
-      m_run = m_new;
 
-      // probabilities p = 2^(s c - m); masked keys get exactly 0
-      float rowsum = 0.f;
-      if (masked) {
+      // probabilities p = 2^(s c - m), written over S in two halves of 64 keys
+      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
-          s[i] = i < lim ? ex2_mufu(fmaf(s[i], c, -m_new)) : 0.f;
-          rowsum += s[i];
+      for (int half = 0; half < 2; ++half) {
+#pragma unroll
+        for (int i = 64 * half; i < 64 * half + 64; ++i) {
+          const float x = fmaf(s[i], c, -m_run);
+          s[i] = masked ? (i < lim ? ex2_mufu(x) : 0.f) : ex2_mufu(x);
+          ps[i % 8] += s[i];
         }
-      } else {
+        if constexpr (FP8) {
+          uint32_t r[16];
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
-          s[i] = ex2_mufu(fmaf(s[i], c, -m_new));
-          rowsum += s[i];
-        }
-      }
-      l_run = l_run * alpha + rowsum;
-
-      // write P over S_h (packed), then signal the MMA warp
-      if constexpr (FP8) {
-        uint32_t r[32];
+          for (int i = 0; i < 16; ++i) {
+            const int k = 64 * half + 4 * i;
+            r[i] = pack_e4m3x4(s[k], s[k + 1], s[k + 2], s[k + 3]);
+          }
+          tmem_st16(t_s + 16 * half, r);
+        } else {
+          uint32_t r[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          r[i] = pack_e4m3x4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]);
-        tmem_st32(t_s, r);
-      } else {
-        uint32_t r[32];
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            r[i] = pack_bf16x2(s[64 * half + 2 * i], s[64 * half + 2 * i + 1]);
+          for (int i = 0; i < 32; ++i) r[i] = pack_bf16x2(s[64 * half + 2 * i], s[64 * half + 2 * i + 1]);
           tmem_st32(t_s + 32 * half, r);
         }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full[h][half]));
+        if (threadIdx.x % 128 == 0) EXATTN_TRACE_EVENT(2 + half, h, j);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full[h]));
+#pragma unroll
+      for (int w = 4; w >= 1; w /= 2)
+#pragma unroll
+        for (int k = 0; k < w; ++k) ps[k] += ps[k + w];
+      l_run += ps[0];
     }
 
     if (ok && nkv_h > 0) {
