@@ -205,7 +205,7 @@ int fa_version(void) { return 100; }
 
 #ifdef EXATTN_TRACE
 // Diagnostic builds only: point the timeline trace at a device buffer of
-// 10 * 2 * kTraceMaxJ int64 and pick the CTA (blockIdx.x + gridDim.x * blockIdx.y) to record.
+// 11 * 2 * kTraceMaxJ int64 and pick the CTA (blockIdx.x + gridDim.x * blockIdx.y) to record.
 FA_API int fa_trace_config(long long* buf, int cta) {
   if (cudaMemcpyToSymbol(g_trace_buf, &buf, sizeof(buf)) != cudaSuccess) return FA_ERR_CUDA;
   if (cudaMemcpyToSymbol(g_trace_cta, &cta, sizeof(cta)) != cudaSuccess) return FA_ERR_CUDA;

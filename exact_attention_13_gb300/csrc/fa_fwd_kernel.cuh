@@ -42,7 +42,7 @@
 namespace exattn {
 
 // Optional timeline trace (build with -DEXATTN_TRACE): one CTA records clock64() at the role
-// hand-offs into a device buffer of 10 x 2 x kTraceMaxJ int64, for profiling the pipeline.
+// hand-offs into a device buffer of 11 x 2 x kTraceMaxJ int64, for profiling the pipeline.
 // Compiled out by default.
 #ifdef EXATTN_TRACE
 __device__ long long* g_trace_buf;
@@ -77,8 +77,33 @@ constexpr float kLn2 = 0.6931471805599453f;
 // up a rounding error (2^-9 relative in bf16) that the threshold-0 schedule avoids (there the
 // row max maps to exactly 1).  On logits spread over +-100 that costs up to ~0.009 in O, enough
 // to cross the 1e-2 gate, so the kernel uses 0.
-constexpr float kRescaleLog2 = 0.0f;
-constexpr int kL2PrefetchBlocks = 6;  // K/V blocks warmed in L2 ahead of the ring
+#ifndef EXATTN_RESCALE_LOG2
+#define EXATTN_RESCALE_LOG2 0.0f
+#endif
+constexpr float kRescaleLog2 = EXATTN_RESCALE_LOG2;
+// Design knobs (compile-time).  The defaults are the measured best on GB300 (A/B over whole
+// launches of the headline shapes): bf16 is MMA-issue-bound and prefers P published in one
+// part with a short L2 prefetch; e4m3 is softmax-bound and gains from PV starting on the first
+// half of P and a deeper prefetch.  -D overrides apply to both operand types.
+#ifndef EXATTN_KV_SLOTS_D128
+#define EXATTN_KV_SLOTS_D128 4
+#endif
+template <bool FP8>
+__host__ __device__ constexpr int l2_prefetch_blocks() {
+#ifdef EXATTN_L2_PREFETCH_BLOCKS
+  return EXATTN_L2_PREFETCH_BLOCKS;
+#else
+  return FP8 ? 6 : 2;
+#endif
+}
+template <bool FP8>
+__host__ __device__ constexpr int p_parts() {
+#ifdef EXATTN_P_HALVES
+  return EXATTN_P_HALVES;
+#else
+  return FP8 ? 2 : 1;
+#endif
+}
 
 struct KernelArgs {
   __nv_bfloat16* o;   // [BH, N, d]
@@ -98,7 +123,7 @@ struct Geo {
   static constexpr int kBoxes = kRowBytes / kSwBytes;       // TMA boxes per 128-row tile
   static constexpr int kBoxElems = kSwBytes / kElem;        // inner box extent (elements)
   static constexpr int kTileBytes = kTileRows * kRowBytes;  // one 128-row operand tile
-  static constexpr int kSlots = (FP8 || D == 64) ? 8 : 5;   // K/V ring depth
+  static constexpr int kSlots = (FP8 || D == 64) ? 8 : EXATTN_KV_SLOTS_D128;  // K/V ring depth
   static constexpr int kQBytes = 2 * kTileBytes;
   static constexpr int kRingBytes = kSlots * kTileBytes;
   static constexpr uint32_t kSwMode = kSwBytes == 128 ? kSwizzle128B : kSwizzle64B;
@@ -159,11 +184,63 @@ __device__ __forceinline__ int kv_blocks_for_tile(int row0, int n) {
   return CAUSAL ? (row0 / kTileRows + 1) : total;
 }
 
+// Softmax numerator of one row: p_i = 2^(s_i c - m) for the 128 keys of the block (keys >= lim
+// are masked to 0 when MASKED), rounded to bf16 (or e4m3) and written over the S columns in TMEM
+// in two halves of 64 keys; after the last half (or after each half when P_PARTS == 2) the warp
+// publishes on the P barrier.  Returns the fp32 sum of the unrounded p.
+template <bool MASKED, bool FP8, int P_PARTS>
+__device__ __forceinline__ float exp_and_publish(float (&s)[128], float c, float m, int lim,
+                                                 uint32_t t_s, uint32_t bar0, uint32_t bar1,
+                                                 int lane) {
+  float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+#pragma unroll
+    for (int i = 64 * half; i < 64 * half + 64; ++i) {
+      const float x = fmaf(s[i], c, -m);
+      float p;
+      if constexpr (MASKED)
+        p = i < lim ? ex2_mufu(x) : 0.f;
+      else
+        p = ex2_mufu(x);
+      s[i] = p;
+      ps[i % 8] += p;
+    }
+    if constexpr (FP8) {
+      uint32_t r[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int k = 64 * half + 4 * i;
+        r[i] = pack_e4m3x4(s[k], s[k + 1], s[k + 2], s[k + 3]);
+      }
+      tmem_st16(t_s + 16 * half, r);
+    } else {
+      uint32_t r[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r[i] = pack_bf16x2(s[64 * half + 2 * i], s[64 * half + 2 * i + 1]);
+      tmem_st32(t_s + 32 * half, r);
+    }
+    if (P_PARTS == 2 || half == 1) {
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(half == 0 ? bar0 : bar1);
+    }
+  }
+#pragma unroll
+  for (int w = 4; w >= 1; w /= 2)
+#pragma unroll
+    for (int k = 0; k < w; ++k) ps[k] += ps[k + w];
+  return ps[0];
+}
+
 template <int D, bool FP8, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const KernelArgs args) {
   using G = Geo<D, FP8>;
+  constexpr int kPHalves = p_parts<FP8>();
+  constexpr int kL2PrefetchBlocks = l2_prefetch_blocks<FP8>();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -323,14 +400,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         EXATTN_TRACE_EVENT(8, h, j);
         const uint32_t v_tile = ring_base + (t % G::kSlots) * G::kTileBytes;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        for (int half = 0; half < kPHalves; ++half) {
           if (!wait_phase(smem_u32(&ctl->p_full[h][half]), j & 1, abort_flag, args.status))
             return false;
           tc_fence_after();
           if (half == 0) EXATTN_TRACE_EVENT(4, h, j);
 #pragma unroll
-          for (int kk = 0; kk < G::kPvSteps / 2; ++kk) {
-            const int kb = half * (G::kPvSteps / 2) + kk;
+          for (int kk = 0; kk < G::kPvSteps / kPHalves; ++kk) {
+            const int kb = half * (G::kPvSteps / kPHalves) + kk;
             const uint64_t dv = smem_desc(v_tile + kb * G::kKeysPerPv * G::kSwBytes,
                                           kTileRows * G::kSwBytes, 8 * G::kSwBytes, G::kSwMode);
             const uint32_t a = tmem + h * 128 + kb * 8;
@@ -444,42 +521,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         l_run *= alpha;
         m_run = m_cand;
       }
+      if (threadIdx.x % 128 == 0) EXATTN_TRACE_EVENT(10, h, j);
 
-      // probabilities p = 2^(s c - m), written over S in two halves of 64 keys
-      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-#pragma unroll
-        for (int i = 64 * half; i < 64 * half + 64; ++i) {
-          const float x = fmaf(s[i], c, -m_run);
-          s[i] = masked ? (i < lim ? ex2_mufu(x) : 0.f) : ex2_mufu(x);
-          ps[i % 8] += s[i];
-        }
-        if constexpr (FP8) {
-          uint32_t r[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int k = 64 * half + 4 * i;
-            r[i] = pack_e4m3x4(s[k], s[k + 1], s[k + 2], s[k + 3]);
-          }
-          tmem_st16(t_s + 16 * half, r);
-        } else {
-          uint32_t r[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = pack_bf16x2(s[64 * half + 2 * i], s[64 * half + 2 * i + 1]);
-          tmem_st32(t_s + 32 * half, r);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full[h][half]));
-        if (threadIdx.x % 128 == 0) EXATTN_TRACE_EVENT(2 + half, h, j);
-      }
-#pragma unroll
-      for (int w = 4; w >= 1; w /= 2)
-#pragma unroll
-        for (int k = 0; k < w; ++k) ps[k] += ps[k + w];
-      l_run += ps[0];
+      // probabilities p = 2^(s c - m), written over S (masked keys give exactly 0); the mask
+      // test lives in its own instantiation so unmasked blocks run a select-free loop
+      const uint32_t pb0 = smem_u32(&ctl->p_full[h][0]);
+      const uint32_t pb1 = smem_u32(&ctl->p_full[h][kPHalves == 2 ? 1 : 0]);
+      const float rowsum =
+          masked ? exp_and_publish<true, FP8, kPHalves>(s, c, m_run, lim, t_s, pb0, pb1, lane)
+                 : exp_and_publish<false, FP8, kPHalves>(s, c, m_run, lim, t_s, pb0, pb1, lane);
+      if (threadIdx.x % 128 == 0) EXATTN_TRACE_EVENT(3, h, j);
+      l_run += rowsum;
     }
 
     if (ok && nkv_h > 0) {
