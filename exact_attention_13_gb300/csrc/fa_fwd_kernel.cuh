@@ -5,7 +5,8 @@
 // online-softmax state (running max m, running sum l) in registers and the unnormalised output
 // in tensor memory ("FlashAttention · InkStack", sections 1.1.2 "Online Softmax" and 2.1; the
 // two-tile ping-pong and TMEM plan of "FlashAttention4 精读", section "新pipeline来overlap matmul
-// 和softmax").  Warp roles (384 threads):
+// 和softmax").  Warp roles (384 threads; a separate correction warpgroup was measured and is
+// slower on GB300, see the rescale note below):
 //
 //   warps 0-3  softmax, Q tile 0     one thread per query row: reads its S row from TMEM,
 //   warps 4-7  softmax, Q tile 1     updates (m, l), rescales its O row when m grew, writes the
@@ -76,7 +77,10 @@ constexpr float kLn2 = 0.6931471805599453f;
 // values above 1 are not exact in bf16/e4m3, so the dominant probability of a peaked row picks
 // up a rounding error (2^-9 relative in bf16) that the threshold-0 schedule avoids (there the
 // row max maps to exactly 1).  On logits spread over +-100 that costs up to ~0.009 in O, enough
-// to cross the 1e-2 gate, so the kernel uses 0.
+// to cross the 1e-2 gate, so the kernel uses 0.  The softmax warps rescale O themselves: a
+// separate correction warpgroup (16 warps; the softmax posts alpha, four warps rescale O while
+// the exponentials run) measured 9-16 % slower on GB300, because the 512-thread register split
+// leaves the softmax 168 registers and the alpha -> O-ready hand-off lands on the MMA's path.
 #ifndef EXATTN_RESCALE_LOG2
 #define EXATTN_RESCALE_LOG2 0.0f
 #endif
@@ -96,6 +100,12 @@ __host__ __device__ constexpr int l2_prefetch_blocks() {
   return FP8 ? 6 : 2;
 #endif
 }
+// Fraction of exponentials evaluated by the FMA polynomial instead of MUFU: one column in every
+// EXATTN_EMU_EVERY of an unmasked block (0 = MUFU only).  On GB300 MUFU does 32 ex2/clk/SM and
+// the softmax is issue-bound, so emulation costs time (1-in-8 measured -5..-7 %); off by default.
+#ifndef EXATTN_EMU_EVERY
+#define EXATTN_EMU_EVERY 0
+#endif
 template <bool FP8>
 __host__ __device__ constexpr int p_parts() {
 #ifdef EXATTN_P_HALVES
@@ -185,10 +195,12 @@ __device__ __forceinline__ int kv_blocks_for_tile(int row0, int n) {
 }
 
 // Softmax numerator of one row: p_i = 2^(s_i c - m) for the 128 keys of the block (keys >= lim
-// are masked to 0 when MASKED), rounded to bf16 (or e4m3) and written over the S columns in TMEM
-// in two halves of 64 keys; after the last half (or after each half when P_PARTS == 2) the warp
-// publishes on the P barrier.  Returns the fp32 sum of the unrounded p.
-template <bool MASKED, bool FP8, int P_PARTS>
+// are masked to 0 when MASKED; with EMU_EVERY > 0 one column in EMU_EVERY of an unmasked block
+// uses the FMA polynomial, "FlashAttention4 精读", section 3.1.3 "partial emulation"), rounded
+// to bf16 (or e4m3) and written over the S columns in TMEM in two halves of 64 keys; after the
+// last half (or after each half when P_PARTS == 2) the warp publishes on the P barrier.  Returns
+// the fp32 sum of the unrounded p.
+template <bool MASKED, bool FP8, int P_PARTS, int EMU_EVERY>
 __device__ __forceinline__ float exp_and_publish(float (&s)[128], float c, float m, int lim,
                                                  uint32_t t_s, uint32_t bar0, uint32_t bar1,
                                                  int lane) {
@@ -201,6 +213,8 @@ __device__ __forceinline__ float exp_and_publish(float (&s)[128], float c, float
       float p;
       if constexpr (MASKED)
         p = i < lim ? ex2_mufu(x) : 0.f;
+      else if constexpr (EMU_EVERY > 0)
+        p = (i % EMU_EVERY == EMU_EVERY - 1) ? ex2_poly(x) : ex2_mufu(x);
       else
         p = ex2_mufu(x);
       s[i] = p;
@@ -528,8 +542,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t pb0 = smem_u32(&ctl->p_full[h][0]);
       const uint32_t pb1 = smem_u32(&ctl->p_full[h][kPHalves == 2 ? 1 : 0]);
       const float rowsum =
-          masked ? exp_and_publish<true, FP8, kPHalves>(s, c, m_run, lim, t_s, pb0, pb1, lane)
-                 : exp_and_publish<false, FP8, kPHalves>(s, c, m_run, lim, t_s, pb0, pb1, lane);
+          masked ? exp_and_publish<true, FP8, kPHalves, 0>(s, c, m_run, lim, t_s, pb0, pb1, lane)
+                 : exp_and_publish<false, FP8, kPHalves, EXATTN_EMU_EVERY>(s, c, m_run, lim, t_s,
+                                                                           pb0, pb1, lane);
       if (threadIdx.x % 128 == 0) EXATTN_TRACE_EVENT(3, h, j);
       l_run += rowsum;
     }
