@@ -69,7 +69,16 @@ constexpr int kThreads = 384;
 constexpr int kTileRows = 128;       // query rows per Q tile, keys per K/V block
 constexpr int kCtaRows = 2 * kTileRows;
 constexpr int kStatusTimeout = 5;    // FA_ERR_DEVICE_TIMEOUT
-constexpr uint64_t kWaitLimitNs = 4ull * 1000 * 1000 * 1000;  // 4 s per wait
+#ifndef EXATTN_WAIT_LIMIT_NS
+#define EXATTN_WAIT_LIMIT_NS 4000000000ull
+#endif
+constexpr uint64_t kWaitLimitNs = EXATTN_WAIT_LIMIT_NS;  // per wait (4 s in the library)
+// Fault injection for the test of the timeout path (test builds only, never in the library):
+// the producer loads the Q tiles and then stops, so the first K/V wait runs out and every role
+// must leave through the abort path.
+#ifndef EXATTN_INJECT_STALL
+#define EXATTN_INJECT_STALL 0
+#endif
 constexpr float kLn2 = 0.6931471805599453f;
 // Rescale threshold (log2 units).  0 rescales whenever a row's max grows; a positive value is the
 // lazy rescale of "FlashAttention4 精读", section 3.1.4 (the page uses 8, a factor 2^8), which
@@ -332,7 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       int issued = 0;
       bool ok = true;
-      for (int t = 0; t < 2 * nkv_load && ok; ++t) {
+      const int n_loads = EXATTN_INJECT_STALL ? 0 : 2 * nkv_load;
+      for (int t = 0; t < n_loads && ok; ++t) {
         const int slot = t % G::kSlots;
         const int round = t / G::kSlots;
         if (round > 0) {
