@@ -103,7 +103,9 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   args.n = N;
   args.c = c;
   args.out_mult = out_mult;
-  dim3 grid((N + kCtaRows - 1) / kCtaRows, bh, 1);
+  const unsigned mblocks = static_cast<unsigned>((N + kCtaRows - 1) / kCtaRows);
+  const dim3 grid = CAUSAL ? dim3(static_cast<unsigned>(bh), mblocks, 1)
+                           : dim3(mblocks, static_cast<unsigned>(bh), 1);
   kern<<<grid, kThreads, smem_request, stream>>>(mq, mk, mv, args);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -153,6 +155,7 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * H > 65535) return FA_ERR_UNSUPPORTED;
   if (N > 0x7FFFFFFF - 2 * kCtaRows) return FA_ERR_UNSUPPORTED;
+  if (causal && (N + kCtaRows - 1) / kCtaRows > 65535) return FA_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
       !aligned(lse, 4) || (status && !aligned(status, 4)))
     return FA_ERR_MISALIGNED;

@@ -275,9 +275,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x % 32;
   const int n = args.n;
   EXATTN_TRACE_SETUP;
-  const int bh = blockIdx.y;
-  // heaviest query blocks first under the causal mask (they see the most keys)
-  const int mblock = CAUSAL ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x;
+  // Launch order.  Non-causal: query blocks of one head are adjacent (x), so the CTAs sharing
+  // that head's K/V run together and re-read it from L2.  Causal: heads are adjacent (x) and
+  // query blocks run from the last (heaviest: it sees every key block) to the first (y), i.e.
+  // longest-processing-time-first over the whole grid ("FlashAttention4 精读", section 3.3).
+  const int bh = CAUSAL ? blockIdx.x : blockIdx.y;
+  const int mblock = CAUSAL ? (gridDim.y - 1 - blockIdx.y) : blockIdx.x;
   const int row0 = mblock * kCtaRows;
   const int nkv0 = kv_blocks_for_tile<CAUSAL>(row0, n);
   const int nkv1 = kv_blocks_for_tile<CAUSAL>(row0 + kTileRows, n);

@@ -62,7 +62,7 @@ typedef enum {
  *   q, k, v : device pointers, [B, H, N, d] of `dtype` (16-byte aligned)
  *   o       : device pointer, [B, H, N, d] bf16 (16-byte aligned)
  *   lse     : device pointer, [B, H, N] fp32 (4-byte aligned)
- *   B, H, N : >= 1, with B * H <= 65535 and N < 2^31 - 256
+ *   B, H, N : >= 1, with B * H <= 65535 and N < 2^31 - 512 (causal: N <= 65535 * 256)
  *   d       : head dimension, 64 or 128
  *   scale   : softmax scale applied to q . k, finite and >= 0 (usually 1/sqrt(d))
  *   causal  : 0 = no mask, nonzero = lower-triangular mask (diagonal included)
