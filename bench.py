@@ -234,8 +234,15 @@ def run_ours(args, w, world, rank, local):
     lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    splits = args.splits
+    workspace = None
+    if splits > 1:
+        workspace = torch.empty(ea.split_workspace_bytes(w.B, w.H, w.N, w.d, splits),
+                                dtype=torch.uint8, device=dev)
+
     def step():
-        ea.fwd(q, k, v, causal=w.causal, scale=w.scale, descale=descale, out=o, lse=lse)
+        ea.fwd(q, k, v, causal=w.causal, scale=w.scale, descale=descale, out=o, lse=lse,
+               num_splits=splits, workspace=workspace)
 
     for _ in range(args.warmup):
         step()
@@ -299,7 +306,7 @@ def run_ours(args, w, world, rank, local):
         s_cmp.wait_event(ev["out"][b])         # the D2H that last read outputs b is done
         with torch.cuda.stream(s_cmp):
             ea.fwd(dq[b], dk[b], dv[b], causal=w.causal, scale=w.scale, descale=descale,
-                   out=do[b], lse=dl[b])
+                   out=do[b], lse=dl[b], num_splits=splits, workspace=workspace)
         ev["cmp"][b].record(s_cmp)
         s_out.wait_event(ev["cmp"][b])
         with torch.cuda.stream(s_out):
@@ -358,6 +365,7 @@ def run_ours(args, w, world, rank, local):
         "config": {"workload": w.name, "shape": w.describe(), "global_batch": w.B * world,
                    "heads": w.H, "seq_len": w.N, "head_dim": w.d, "causal": w.causal,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "key_splits": args.splits,
                    "l2": "inputs larger than L2 (no flush)" if 3 * q.numel() * q.element_size()
                    > 129e6 else "inputs smaller than L2"},
         "pct_of_peak": 100.0 * achieved / peak,
@@ -368,7 +376,7 @@ def run_ours(args, w, world, rank, local):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
                 "pipelining": "2 buffer sets; H2D, kernel, D2H on 3 streams"},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if args.splits > 1 else 1),
     }
     if not args.no_cpu_baseline:
         tf, dt, cores, sample = oracle_sample_rate(inp, w, target_s=args.cpu_s)
@@ -384,6 +392,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--splits", type=int, default=1,
+                    help="key splits per query tile (split-KV + merge kernel)")
     ap.add_argument("--cpu-s", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--ref-step-s", type=float, default=4.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -38,6 +38,12 @@ SIGNATURES = {
     "fa_fwd_ex": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
                              _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_float, _c.c_int,
                              _c.c_int, _c.c_void_p, _c.c_void_p]),
+    "fa_fwd_split": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                                _c.c_void_p, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_float,
+                                _c.c_int, _c.c_int, _c.c_int, _c.c_void_p, _c.c_size_t,
+                                _c.c_void_p, _c.c_void_p]),
+    "fa_fwd_split_workspace_bytes": (_c.c_size_t, [_c.c_int, _c.c_int, _c.c_int, _c.c_int,
+                                                   _c.c_int]),
     "fa_device_status": (_c.c_int, [_c.c_int, _c.POINTER(_c.c_int)]),
     "fa_status_string": (_c.c_char_p, [_c.c_int]),
     "fa_version": (_c.c_int, []),
@@ -108,6 +114,19 @@ def fa_fwd_ex(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, scale, causal, dt
                            dtype, ctypes.byref(opts), stream)
 
 
+def fa_fwd_split(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, scale, causal, dtype,
+                 num_splits, workspace_ptr, workspace_bytes, descale=(1.0, 1.0, 1.0),
+                 status_ptr=None, stream=None) -> int:
+    opts = FwdOpts(float(descale[0]), float(descale[1]), float(descale[2]), status_ptr)
+    return lib().fa_fwd_split(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, scale,
+                              int(causal), dtype, int(num_splits), workspace_ptr,
+                              int(workspace_bytes), ctypes.byref(opts), stream)
+
+
+def split_workspace_bytes(B: int, H: int, N: int, d: int, num_splits: int) -> int:
+    return int(lib().fa_fwd_split_workspace_bytes(B, H, N, d, num_splits))
+
+
 def device_status(clear: bool = True) -> int:
     out = ctypes.c_int(0)
     _check(lib().fa_device_status(int(clear), ctypes.byref(out)), "fa_device_status")
@@ -119,12 +138,15 @@ def version() -> int:
 
 
 def fwd(q, k, v, causal: bool = False, scale: float | None = None, descale=None, out=None,
-        lse=None, status=None):
+        lse=None, status=None, num_splits: int = 1, workspace=None):
     """Attention forward on torch CUDA tensors [B, H, N, d]; returns (o bf16, lse fp32).
 
     ``descale`` = (dq, dk, dv) for float8_e4m3fn operands.  ``out``/``lse`` may be given
     (contiguous, right shape and dtype) to avoid allocation.  ``status`` is an optional int32
     CUDA tensor of one element the kernel sets to FA_ERR_DEVICE_TIMEOUT if a wait runs out.
+    ``num_splits`` > 1 splits each query tile's keys over that many CTAs and merges the partial
+    results (fa_fwd_split); its scratch is ``workspace`` (a CUDA tensor of at least
+    split_workspace_bytes(...) bytes) or, if None, a temporary allocated here by torch.
     """
     import torch
 
@@ -157,9 +179,22 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, descale=None,
     st = status.data_ptr() if status is not None else None
     stream = torch.cuda.current_stream(q.device).cuda_stream
     with torch.cuda.device(q.device):
-        rc = fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                       B, H, N, d, float(scale), causal, dtype, (dq, dk, dv), st, stream)
-    _check(rc, "fa_fwd_ex")
+        if num_splits == 1:
+            rc = fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                           lse.data_ptr(), B, H, N, d, float(scale), causal, dtype, (dq, dk, dv),
+                           st, stream)
+            _check(rc, "fa_fwd_ex")
+            return out, lse
+        need = split_workspace_bytes(B, H, N, d, num_splits)
+        if need == 0:
+            raise ValueError(f"invalid split configuration (num_splits={num_splits}, d={d})")
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        nbytes = workspace.numel() * workspace.element_size()
+        rc = fa_fwd_split(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                          lse.data_ptr(), B, H, N, d, float(scale), causal, dtype, num_splits,
+                          workspace.data_ptr(), nbytes, (dq, dk, dv), st, stream)
+    _check(rc, "fa_fwd_split")
     return out, lse
 
 

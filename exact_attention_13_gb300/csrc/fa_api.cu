@@ -15,6 +15,14 @@ namespace exattn {
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr int kMaxSplits = 16;
+
+// Bytes of the key-split partials: O_s [splits, B*H, N, d] and LSE_s [splits, B*H, N], fp32.
+size_t split_workspace_bytes(int B, int H, int N, int d, int splits) {
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  const size_t bytes = static_cast<size_t>(splits) * rows * (static_cast<size_t>(d) + 1) * 4;
+  return (bytes + 255) / 256 * 256;
+}
 
 // Per-device status word the kernel writes when a bounded wait runs out (fa_fwd callers that
 // pass no status pointer of their own).
@@ -75,7 +83,8 @@ bool encode_operand_map(CUtensorMap* map, const void* ptr, int elem_bytes, int d
 
 template <int D, bool FP8, bool CAUSAL>
 int launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
-           float c, float out_mult, int* status, cudaStream_t stream) {
+           float c, float out_mult, int* status, int splits, float* o_part, float* lse_part,
+           cudaStream_t stream) {
   constexpr int elem = FP8 ? 1 : 2;
   CUtensorMap mq, mk, mv;
   const int bh = B * H;
@@ -100,21 +109,75 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   args.lse = lse;
   args.status = status ? status : library_status_ptr(dev);
   if (!args.status) return FA_ERR_CUDA;
+  args.o_part = o_part;
+  args.lse_part = lse_part;
   args.n = N;
+  args.bh = bh;
   args.c = c;
   args.out_mult = out_mult;
   const unsigned mblocks = static_cast<unsigned>((N + kCtaRows - 1) / kCtaRows);
-  const dim3 grid = CAUSAL ? dim3(static_cast<unsigned>(bh), mblocks, 1)
-                           : dim3(mblocks, static_cast<unsigned>(bh), 1);
+  const unsigned z = static_cast<unsigned>(splits);
+  const dim3 grid = CAUSAL ? dim3(static_cast<unsigned>(bh), mblocks, z)
+                           : dim3(mblocks, static_cast<unsigned>(bh), z);
   kern<<<grid, kThreads, smem_request, stream>>>(mq, mk, mv, args);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 template <int D, bool FP8>
 int launch_mask(int causal, const void* q, const void* k, const void* v, void* o, float* lse,
-                int B, int H, int N, float c, float om, int* st, cudaStream_t s) {
-  return causal ? launch<D, FP8, true>(q, k, v, o, lse, B, H, N, c, om, st, s)
-                : launch<D, FP8, false>(q, k, v, o, lse, B, H, N, c, om, st, s);
+                int B, int H, int N, float c, float om, int* st, int splits, float* op,
+                float* lp, cudaStream_t s) {
+  return causal ? launch<D, FP8, true>(q, k, v, o, lse, B, H, N, c, om, st, splits, op, lp, s)
+                : launch<D, FP8, false>(q, k, v, o, lse, B, H, N, c, om, st, splits, op, lp, s);
+}
+
+// Merge of key splits ("FlashAttention · InkStack", section 2.2: key blocks can be processed
+// independently and merged associatively).  Each split s left O_s (normalised by its own sum)
+// and LSE_s; the merge is LSE = log sum_s e^LSE_s and O = sum_s e^(LSE_s - LSE) O_s, evaluated
+// around the largest LSE_s.  One warp per query row, D / 32 consecutive columns per lane.
+template <int D>
+__global__ void __launch_bounds__(256) combine_splits_kernel(const float* __restrict__ o_part,
+                                                             const float* __restrict__ lse_part,
+                                                             __nv_bfloat16* __restrict__ o,
+                                                             float* __restrict__ lse, int splits,
+                                                             long long rows) {
+  constexpr int kPer = D / 32;
+  const long long row = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+  if (row >= rows) return;
+  const int lane = threadIdx.x % 32;
+  float m = -INFINITY;
+  for (int sp = 0; sp < splits; ++sp) m = fmaxf(m, lse_part[sp * rows + row]);
+  float acc[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+  float l = 0.f;
+  for (int sp = 0; sp < splits; ++sp) {
+    const float ls = lse_part[sp * rows + row];
+    const float w = ls == -INFINITY ? 0.f : expf(ls - m);
+    l += w;
+    const float* src = o_part + (static_cast<size_t>(sp) * rows + row) * D + lane * kPer;
+#pragma unroll
+    for (int i = 0; i < kPer; i += 2) {
+      const float2 x = *reinterpret_cast<const float2*>(src + i);
+      acc[i] = fmaf(w, x.x, acc[i]);
+      acc[i + 1] = fmaf(w, x.y, acc[i + 1]);
+    }
+  }
+  const float inv = 1.f / l;
+  __nv_bfloat16* dst = o + row * D + lane * kPer;
+#pragma unroll
+  for (int i = 0; i < kPer; i += 2)
+    *reinterpret_cast<uint32_t*>(dst + i) = pack_bf16x2(acc[i] * inv, acc[i + 1] * inv);
+  if (lane == 0) lse[row] = m + logf(l);
+}
+
+template <int D>
+int launch_combine(const float* o_part, const float* lse_part, void* o, float* lse, int splits,
+                   long long rows, cudaStream_t s) {
+  const long long blocks = (rows + 7) / 8;
+  combine_splits_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+      o_part, lse_part, static_cast<__nv_bfloat16*>(o), lse, splits, rows);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -128,17 +191,19 @@ __global__ void exp2_probe_kernel(const float* x, float* y, long long n, int mod
 }  // namespace
 }  // namespace exattn
 
-using namespace exattn;
+namespace exattn {
+namespace {
 
-extern "C" {
-
-int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-              int N, int d, float scale, int causal, int dtype, const fa_fwd_opts* opts,
-              void* stream) {
+// Shared argument checks and dispatch of fa_fwd_ex / fa_fwd_split.  splits == 1 writes O and
+// LSE directly; splits > 1 writes per-split partials into `workspace`, then merges them.
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+             int N, int d, float scale, int causal, int dtype, const fa_fwd_opts* opts,
+             int splits, void* workspace, size_t workspace_bytes, void* stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
   if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP8_E4M3) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
+  if (splits < 1 || splits > kMaxSplits) return FA_ERR_INVALID_ARG;
   float dq = 1.f, dk = 1.f, dv = 1.f;
   int* status = nullptr;
   if (opts) {
@@ -156,6 +221,15 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
   if (static_cast<long long>(B) * H > 65535) return FA_ERR_UNSUPPORTED;
   if (N > 0x7FFFFFFF - 2 * kCtaRows) return FA_ERR_UNSUPPORTED;
   if (causal && (N + kCtaRows - 1) / kCtaRows > 65535) return FA_ERR_UNSUPPORTED;
+  float* o_part = nullptr;
+  float* lse_part = nullptr;
+  if (splits > 1) {
+    const size_t need = split_workspace_bytes(B, H, N, d, splits);
+    if (!workspace || workspace_bytes < need) return FA_ERR_INVALID_ARG;
+    if (!aligned(workspace, 16)) return FA_ERR_MISALIGNED;
+    o_part = static_cast<float*>(workspace);
+    lse_part = o_part + static_cast<size_t>(splits) * B * H * N * d;
+  }
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
       !aligned(lse, 4) || (status && !aligned(status, 4)))
     return FA_ERR_MISALIGNED;
@@ -163,12 +237,51 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
   if (!std::isfinite(c) || c > 3.0e38) return FA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const float cf = static_cast<float>(c);
+  int rc;
   if (dtype == FA_DTYPE_BF16) {
-    if (d == 64) return launch_mask<64, false>(causal, q, k, v, o, lse, B, H, N, cf, 1.f, status, s);
-    return launch_mask<128, false>(causal, q, k, v, o, lse, B, H, N, cf, 1.f, status, s);
+    rc = d == 64 ? launch_mask<64, false>(causal, q, k, v, o, lse, B, H, N, cf, 1.f, status,
+                                          splits, o_part, lse_part, s)
+                 : launch_mask<128, false>(causal, q, k, v, o, lse, B, H, N, cf, 1.f, status,
+                                           splits, o_part, lse_part, s);
+  } else {
+    rc = d == 64 ? launch_mask<64, true>(causal, q, k, v, o, lse, B, H, N, cf, dv, status,
+                                         splits, o_part, lse_part, s)
+                 : launch_mask<128, true>(causal, q, k, v, o, lse, B, H, N, cf, dv, status,
+                                          splits, o_part, lse_part, s);
   }
-  if (d == 64) return launch_mask<64, true>(causal, q, k, v, o, lse, B, H, N, cf, dv, status, s);
-  return launch_mask<128, true>(causal, q, k, v, o, lse, B, H, N, cf, dv, status, s);
+  if (rc != FA_OK || splits == 1) return rc;
+  const long long rows = static_cast<long long>(B) * H * N;
+  return d == 64 ? launch_combine<64>(o_part, lse_part, o, lse, splits, rows, s)
+                 : launch_combine<128>(o_part, lse_part, o, lse, splits, rows, s);
+}
+
+}  // namespace
+}  // namespace exattn
+
+using namespace exattn;
+
+extern "C" {
+
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+              int N, int d, float scale, int causal, int dtype, const fa_fwd_opts* opts,
+              void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, opts, 1, nullptr, 0,
+                  stream);
+}
+
+size_t fa_fwd_split_workspace_bytes(int B, int H, int N, int d, int num_splits) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128) || num_splits < 1 ||
+      num_splits > kMaxSplits)
+    return 0;
+  return split_workspace_bytes(B, H, N, d, num_splits);
+}
+
+int fa_fwd_split(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int d, float scale, int causal, int dtype, int num_splits,
+                 void* workspace, size_t workspace_bytes, const fa_fwd_opts* opts,
+                 void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, opts, num_splits,
+                  workspace, workspace_bytes, stream);
 }
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,

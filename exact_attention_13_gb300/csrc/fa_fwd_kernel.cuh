@@ -125,10 +125,13 @@ __host__ __device__ constexpr int p_parts() {
 }
 
 struct KernelArgs {
-  __nv_bfloat16* o;   // [BH, N, d]
-  float* lse;         // [BH, N]
+  __nv_bfloat16* o;   // [BH, N, d]            (one key split)
+  float* lse;         // [BH, N]               (one key split)
+  float* o_part;      // [splits, BH, N, d]    (several key splits: O of each split, fp32)
+  float* lse_part;    // [splits, BH, N]       (several key splits: LSE of each split)
   int* status;        // device status word (never null when launched by the library)
   int n;              // keys = queries per head
+  int bh;             // batch * heads
   float c;            // scale * log2(e) * descale_q * descale_k
   float out_mult;     // descale_v (1 for bf16)
 };
@@ -282,8 +285,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bh = CAUSAL ? blockIdx.x : blockIdx.y;
   const int mblock = CAUSAL ? (gridDim.y - 1 - blockIdx.y) : blockIdx.x;
   const int row0 = mblock * kCtaRows;
-  const int nkv0 = kv_blocks_for_tile<CAUSAL>(row0, n);
-  const int nkv1 = kv_blocks_for_tile<CAUSAL>(row0 + kTileRows, n);
+  const int nkv0_all = kv_blocks_for_tile<CAUSAL>(row0, n);
+  const int nkv1_all = kv_blocks_for_tile<CAUSAL>(row0 + kTileRows, n);
+  // Key split (blockIdx.z of gridDim.z): this CTA visits key blocks [jb, jb + nkv_h) of tile h;
+  // a tile whose range is empty in this split only reports an empty partial result.
+  const int nsplit = gridDim.z;
+  const int nkv_all = nkv0_all > nkv1_all ? nkv0_all : nkv1_all;
+  const int jb = static_cast<int>(static_cast<long long>(blockIdx.z) * nkv_all / nsplit);
+  const int je = static_cast<int>(static_cast<long long>(blockIdx.z + 1) * nkv_all / nsplit);
+  const int nkv0 = max(0, min(je, nkv0_all) - jb);
+  const int nkv1 = max(0, min(je, nkv1_all) - jb);
   const int nkv_load = nkv0 > nkv1 ? nkv0 : nkv1;
 
   // ---------------------------------------------------------------- setup
@@ -339,8 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // L2 warm-up of the first K/V blocks; the loop keeps it kL2PrefetchBlocks ahead
       for (int j = 0; j < kL2PrefetchBlocks && j < nkv_load; ++j)
         for (int b = 0; b < G::kBoxes; ++b) {
-          tma_prefetch_l2_3d(&map_k, b * G::kBoxElems, j * kTileRows, bh);
-          tma_prefetch_l2_3d(&map_v, b * G::kBoxElems, j * kTileRows, bh);
+          tma_prefetch_l2_3d(&map_k, b * G::kBoxElems, (jb + j) * kTileRows, bh);
+          tma_prefetch_l2_3d(&map_v, b * G::kBoxElems, (jb + j) * kTileRows, bh);
         }
       int issued = 0;
       bool ok = true;
@@ -360,11 +371,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* dst = s_ring + slot * G::kTileBytes;
         for (int b = 0; b < G::kBoxes; ++b)
           tma_load_3d_hint(smem_u32(dst + b * kTileRows * G::kSwBytes), map, fbar,
-                           b * G::kBoxElems, (t >> 1) * kTileRows, bh, keep);
+                           b * G::kBoxElems, (jb + (t >> 1)) * kTileRows, bh, keep);
         const int jp = (t >> 1) + kL2PrefetchBlocks;
         if (jp < nkv_load)
           for (int b = 0; b < G::kBoxes; ++b)
-            tma_prefetch_l2_3d(map, b * G::kBoxElems, jp * kTileRows, bh);
+            tma_prefetch_l2_3d(map, b * G::kBoxElems, (jb + jp) * kTileRows, bh);
         ++issued;
       }
       if (!ok) {
@@ -476,6 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = warp / 4;
     const int w4 = warp % 4;
     const int nkv_h = h == 0 ? nkv0 : nkv1;
+    const int nkv_h_all = h == 0 ? nkv0_all : nkv1_all;
     const int r_local = w4 * 32 + lane;        // TMEM lane == row within the tile
     const int row = row0 + h * kTileRows + r_local;
     const uint32_t lane_addr = static_cast<uint32_t>(w4 * 32) << 16;
@@ -506,11 +518,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) s[cb * 32 + i] = __uint_as_float(r[cb][i]);
       }
       // masks: keys past the end of the sequence, and the causal diagonal block
-      const int key0 = j * kTileRows;
-      const bool masked = (key0 + kTileRows > n) || (CAUSAL && j == nkv_h - 1);
+      const int jg = jb + j;  // block index within the head
+      const int key0 = jg * kTileRows;
+      const bool diag = CAUSAL && jg == nkv_h_all - 1;
+      const bool masked = (key0 + kTileRows > n) || diag;
       int lim = kTileRows;  // keys < lim are visible to this row
       if (masked) {
-        const int lim_c = (CAUSAL && j == nkv_h - 1) ? r_local + 1 : kTileRows;
+        const int lim_c = diag ? r_local + 1 : kTileRows;
         lim = min(n - key0, lim_c);
 #pragma unroll
         for (int i = 0; i < 128; ++i)
@@ -569,28 +583,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const float inv_l = args.out_mult / l_run;
         const bool live = row < n;
-        __nv_bfloat16* orow = args.o + (static_cast<size_t>(bh) * n + (live ? row : 0)) * D;
+        const float lse_row = (m_run + lg2_mufu(l_run)) * kLn2;
+        if (nsplit == 1) {
+          __nv_bfloat16* orow = args.o + (static_cast<size_t>(bh) * n + (live ? row : 0)) * D;
 #pragma unroll
-        for (int cb = 0; cb < D / 32; ++cb) {
-          uint32_t r[32];
-          tmem_ld32(t_o + cb * 32, r);
-          tmem_ld_wait();
-          uint32_t packed[16];
+          for (int cb = 0; cb < D / 32; ++cb) {
+            uint32_t r[32];
+            tmem_ld32(t_o + cb * 32, r);
+            tmem_ld_wait();
+            uint32_t packed[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            packed[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l,
-                                    __uint_as_float(r[2 * i + 1]) * inv_l);
-          if (live) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + cb * 32);
+            for (int i = 0; i < 16; ++i)
+              packed[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l,
+                                      __uint_as_float(r[2 * i + 1]) * inv_l);
+            if (live) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + cb * 32);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
-                                  packed[4 * i + 3]);
+              for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                    packed[4 * i + 3]);
+            }
           }
+          if (live) args.lse[static_cast<size_t>(bh) * n + row] = lse_row;
+        } else {
+          // this split's normalised output and log-sum-exp, merged later by the combine kernel
+          const size_t prow = (static_cast<size_t>(blockIdx.z) * args.bh + bh) * n + (live ? row : 0);
+          float* orow = args.o_part + prow * D;
+#pragma unroll
+          for (int cb = 0; cb < D / 32; ++cb) {
+            uint32_t r[32];
+            tmem_ld32(t_o + cb * 32, r);
+            tmem_ld_wait();
+            if (live) {
+              float4* dst = reinterpret_cast<float4*>(orow + cb * 32);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                dst[i] = make_float4(__uint_as_float(r[4 * i]) * inv_l,
+                                     __uint_as_float(r[4 * i + 1]) * inv_l,
+                                     __uint_as_float(r[4 * i + 2]) * inv_l,
+                                     __uint_as_float(r[4 * i + 3]) * inv_l);
+            }
+          }
+          if (live) args.lse_part[prow] = lse_row;
         }
-        if (live)
-          args.lse[static_cast<size_t>(bh) * n + row] = (m_run + lg2_mufu(l_run)) * kLn2;
       }
+    } else if (ok && nsplit > 1 && row < n) {
+      // empty key range in this split: contributes nothing to the merge
+      const size_t prow = (static_cast<size_t>(blockIdx.z) * args.bh + bh) * n + row;
+      float4* dst = reinterpret_cast<float4*>(args.o_part + prow * D);
+#pragma unroll
+      for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      args.lse_part[prow] = -INFINITY;
     }
     tc_fence_before();
   }

@@ -33,6 +33,8 @@
 #ifndef EXACT_ATTENTION_H
 #define EXACT_ATTENTION_H
 
+#include <stddef.h>
+
 #if defined(__GNUC__)
 #define FA_API __attribute__((visibility("default")))
 #else
@@ -92,6 +94,29 @@ typedef struct {
 FA_API int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
               int N, int d, float scale, int causal, int dtype, const fa_fwd_opts* opts,
               void* stream);
+
+/*
+ * Key-split ("split-KV") variant of fa_fwd_ex.  The key blocks each query tile visits are
+ * divided into `num_splits` contiguous ranges processed by separate CTAs (more parallelism when
+ * B * H * ceil(N / 256) is small next to the GPU's SM count); each range leaves its normalised
+ * output and log-sum-exp in `workspace`, and a second kernel merges the ranges with the
+ * associative log-sum-exp merge ("FlashAttention · InkStack", section 2.2: independent key
+ * blocks merged by an associative operation; the (m, l, U) recurrence of section 1.1.2).
+ *   num_splits      : 1..16 (1 = fa_fwd_ex; workspace may then be NULL)
+ *   workspace       : caller-owned device scratch, 16-byte aligned, at least
+ *                     fa_fwd_split_workspace_bytes(B, H, N, d, num_splits) bytes; its contents
+ *                     on entry do not matter and are undefined on return
+ * Other arguments, layouts and errors as fa_fwd_ex; too small a workspace is
+ * FA_ERR_INVALID_ARG.  The result equals fa_fwd_ex's up to fp32 rounding.
+ */
+FA_API int fa_fwd_split(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int H, int N, int d, float scale, int causal, int dtype, int num_splits,
+                        void* workspace, size_t workspace_bytes, const fa_fwd_opts* opts,
+                        void* stream);
+
+/* Workspace bytes fa_fwd_split needs: num_splits * B * H * N * (d + 1) * 4, rounded up to 256;
+ * 0 for invalid arguments. */
+FA_API size_t fa_fwd_split_workspace_bytes(int B, int H, int N, int d, int num_splits);
 
 /*
  * Read, and if `clear` is nonzero reset to FA_OK, the library's status word on the current

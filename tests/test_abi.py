@@ -77,3 +77,23 @@ def test_debug_exp2_checks(lib):
     assert lib.fa_debug_exp2(None, None, 10, 0, None) == ea.FA_ERR_INVALID_ARG
     assert lib.fa_debug_exp2(FAKE, FAKE, 10, 2, None) == ea.FA_ERR_INVALID_ARG
     assert lib.fa_debug_exp2(FAKE, FAKE, 0, 0, None) == ea.FA_OK
+
+
+def test_split_workspace_bytes(lib):
+    assert ea.split_workspace_bytes(1, 2, 300, 128, 3) == (3 * 2 * 300 * 129 * 4 + 255) // 256 * 256
+    assert ea.split_workspace_bytes(1, 1, 1, 64, 1) == 512  # 65 floats -> 260 B -> 512
+    for bad in ((0, 1, 8, 64, 2), (1, 1, 8, 96, 2), (1, 1, 8, 64, 0), (1, 1, 8, 64, 17)):
+        assert ea.split_workspace_bytes(*bad) == 0
+
+
+@pytest.mark.parametrize("splits,ws,nbytes,want", [
+    (0, FAKE, 1 << 30, ea.FA_ERR_INVALID_ARG),
+    (17, FAKE, 1 << 30, ea.FA_ERR_INVALID_ARG),
+    (2, 0, 1 << 30, ea.FA_ERR_INVALID_ARG),
+    (2, FAKE, 1024, ea.FA_ERR_INVALID_ARG),
+    (2, FAKE + 4, 1 << 30, ea.FA_ERR_MISALIGNED),
+])
+def test_split_host_checks(lib, splits, ws, nbytes, want):
+    rc = ea.fa_fwd_split(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 128, 0.1, 0, 0, splits,
+                         ws, nbytes, (1.0, 1.0, 1.0), None, None)
+    assert rc == want

@@ -75,6 +75,10 @@ WORKLOADS = {
                                            "bf16", 1003, note="long sequence"),
     "b2h32n16384d128_e4m3": Workload("b2h32n16384d128_e4m3", 2, 32, 16384, 128, False, "e4m3",
                                      1004, note="fp8 operands, per-tensor descale"),
+    # not one of the method's benchmark shapes: a single long sequence with too few query blocks
+    # to fill the GPU, where splitting the keys over CTAs (split-KV) pays
+    "b1h1n16384d128_bf16": Workload("b1h1n16384d128_bf16", 1, 1, 16384, 128, False, "bf16", 1100,
+                                    note="64 CTAs without key splits"),
 }
 
 HEADLINE = "b2h32n8192d128_bf16"
