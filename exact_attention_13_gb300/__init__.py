@@ -44,6 +44,10 @@ SIGNATURES = {
                                 _c.c_void_p, _c.c_void_p]),
     "fa_fwd_split_workspace_bytes": (_c.c_size_t, [_c.c_int, _c.c_int, _c.c_int, _c.c_int,
                                                    _c.c_int]),
+    "fa_fwd_split_noalloc": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                                        _c.c_void_p, _c.c_int, _c.c_int, _c.c_int, _c.c_int,
+                                        _c.c_float, _c.c_int, _c.c_int, _c.c_int, _c.c_void_p,
+                                        _c.c_void_p]),
     "fa_device_status": (_c.c_int, [_c.c_int, _c.POINTER(_c.c_int)]),
     "fa_status_string": (_c.c_char_p, [_c.c_int]),
     "fa_version": (_c.c_int, []),
@@ -121,6 +125,17 @@ def fa_fwd_split(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, scale, causal,
     return lib().fa_fwd_split(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, scale,
                               int(causal), dtype, int(num_splits), workspace_ptr,
                               int(workspace_bytes), ctypes.byref(opts), stream)
+
+
+def fa_fwd_split_noalloc(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, scale, causal, dtype,
+                         num_splits, descale=(1.0, 1.0, 1.0), status_ptr=None,
+                         stream=None) -> int:
+    """Key-split forward whose partials use the library's fixed device scratch (no allocation
+    anywhere); see fa_fwd_split_noalloc in include/exact_attention.h for the limits."""
+    opts = FwdOpts(float(descale[0]), float(descale[1]), float(descale[2]), status_ptr)
+    return lib().fa_fwd_split_noalloc(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, scale,
+                                      int(causal), dtype, int(num_splits), ctypes.byref(opts),
+                                      stream)
 
 
 def split_workspace_bytes(B: int, H: int, N: int, d: int, num_splits: int) -> int:

@@ -340,3 +340,58 @@ int fa_debug_exp2(const float* x, float* y, long long n, int mode, void* stream)
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------------
+// Key-split forward without any allocation (fa_fwd_split_noalloc).
+//
+// Some callers cannot allocate device memory at call time: a plug-in running inside a host that
+// owns every byte of the GPU's memory and forbids libraries from allocating, or a serving loop
+// that must not stall or fail on an allocation in the middle of a request.  For them the split
+// partials live in one fixed, file-scope scratch array instead of a caller-provided workspace.
+// The array is part of the library's device image: every GPU that loads the library holds its
+// 64 MiB until the process exits, whether or not this entry point is ever called.
+// ---------------------------------------------------------------------------------------------
+namespace exattn {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t{64} << 20;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device.  In host code the array's name is
+// only a host-side stand-in, so the address is looked up with cudaGetSymbolAddress, once per
+// device, while that device is current; the first call on each device does this set-up.
+void* noalloc_scratch(int dev) {
+  static std::atomic<void*> cache[kMaxDevices];
+  void* p = cache[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  void* addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || !addr) return nullptr;
+  cache[dev].store(addr, std::memory_order_release);
+  return addr;
+}
+
+}  // namespace
+}  // namespace exattn
+
+extern "C" {
+
+int fa_fwd_split_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int N, int d, float scale, int causal, int dtype, int num_splits,
+                         const fa_fwd_opts* opts, void* stream) {
+  using namespace exattn;
+  if (B < 1 || H < 1 || N < 1 || num_splits < 1 || num_splits > kMaxSplits)
+    return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  // the partials must fit in the fixed scratch; larger problems are refused, never truncated
+  if (num_splits > 1 && split_workspace_bytes(B, H, N, d, num_splits) > kNoAllocScratchBytes)
+    return FA_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  void* scratch = noalloc_scratch(dev);
+  if (!scratch) return FA_ERR_CUDA;
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, opts, num_splits, scratch,
+                  kNoAllocScratchBytes, stream);
+}
+
+}  // extern "C"

@@ -119,6 +119,31 @@ FA_API int fa_fwd_split(const void* q, const void* k, const void* v, void* o, fl
 FA_API size_t fa_fwd_split_workspace_bytes(int B, int H, int N, int d, int num_splits);
 
 /*
+ * fa_fwd_split without any allocation, for callers that cannot allocate device memory when they
+ * call: a plug-in whose host owns all of the GPU's memory and forbids libraries from allocating,
+ * or a serving loop that must not stall or fail on an allocation mid-request.  The paper has no
+ * counterpart of this entry point; it is an interface convenience of this library.
+ *
+ * Instead of a caller workspace, the split partials live in a fixed 64 MiB scratch array inside
+ * the library's device image (every GPU that loads the library holds it until the process
+ * exits).  The caller still passes inputs and outputs.  No call allocates or frees memory.
+ *   - The first call on a device looks up the scratch's device address (cudaGetSymbolAddress,
+ *     with that device current); make that first call before any stream capture.
+ *   - Problems whose partials need more than 64 MiB, i.e.
+ *     fa_fwd_split_workspace_bytes(B, H, N, d, num_splits) > 64 MiB, return FA_ERR_UNSUPPORTED
+ *     and launch nothing.  num_splits == 1 needs no scratch and behaves as fa_fwd_ex.
+ *   - Every call on a device shares the one array and leaves its last contents there; nothing in
+ *     it needs to start at zero (every partial is written before it is read).  Calls whose
+ *     kernels overlap on the GPU (concurrent streams on the same device) race on the array and
+ *     give undefined results: serialise them.
+ * Other arguments, layouts and errors as fa_fwd_split.
+ */
+FA_API int fa_fwd_split_noalloc(const void* q, const void* k, const void* v, void* o,
+                                float* lse, int B, int H, int N, int d, float scale, int causal,
+                                int dtype, int num_splits, const fa_fwd_opts* opts,
+                                void* stream);
+
+/*
  * Read, and if `clear` is nonzero reset to FA_OK, the library's status word on the current
  * device.  Synchronises the device first.  Writes FA_OK or FA_ERR_DEVICE_TIMEOUT to *out.
  * Returns an fa_status for the call itself.
