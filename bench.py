@@ -176,6 +176,23 @@ def measured_traffic(workload: str, override):
     return ent.get("dram_bytes_per_launch")
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest value of x over all ranks (the slowest rank's time); x itself when alone."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank: float, world: int, ms_slowest: float) -> float:
+    """Whole-job throughput: every rank's work (weak scaling) over the slowest rank's time."""
+    return world * flops_per_rank / (ms_slowest * 1e-3) / 1e12
+
+
 def init_dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -267,13 +284,7 @@ def run_ours(args, w, world, rank, local):
         barrier()
     ms = start.elapsed_time(end) / args.steps
     clocks = clk.summary()
-    ms_max = ms
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, world, dev)
     assert ea.device_status() == 0, "device wait timed out during the bench"
 
     # ---- end to end: pinned host inputs -> device -> attention -> host outputs, per step.
@@ -326,20 +337,14 @@ def run_ours(args, w, world, rank, local):
     s_out.wait_stream(s_cmp)
     e_end.record(s_out)
     torch.cuda.synchronize()
-    e_ms = e_start.elapsed_time(e_end) / args.steps
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e_ms = float(t.item())
+    e_ms = max_over_ranks(e_start.elapsed_time(e_end) / args.steps, world, dev)
     assert ea.device_status() == 0, "device wait timed out during the end-to-end run"
     h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
     d2h = oh[0].numel() * oh[0].element_size() + lh[0].numel() * lh[0].element_size()
 
     flops_rank = w.flops
-    value = world * flops_rank / (ms_max * 1e-3) / 1e12
-    e2e_value = world * flops_rank / (e_ms * 1e-3) / 1e12
+    value = job_tflops(flops_rank, world, ms_max)
+    e2e_value = job_tflops(flops_rank, world, e_ms)
 
     if rank != 0:
         return
