@@ -85,6 +85,10 @@ typedef struct {
     double scale;
     int causal;
     double dq, dk, dv;
+    /* optional per-block descales [B*H, nblk] (values = code * descale of the row's block of
+     * blk_rows rows); NULL: the per-tensor dq, dk, dv apply */
+    const double *dq_blk, *dk_blk, *dv_blk;
+    int64_t blk_rows, nblk;
     const int64_t* rows; /* NULL: every row 0..N-1 */
     int64_t n_rows;
     double* o;   /* [B*H, n_rows, d] */
@@ -119,10 +123,30 @@ static void run_item(job_t* jb, int64_t item, double* Kh, double* Vh, double* qr
     /* this head's keys and values, decoded once per work item */
     load_elems(jb, jb->k, head_off, N * d, Kh);
     load_elems(jb, jb->v, head_off, N * d, Vh);
+    if (jb->dk_blk)
+        for (int64_t j = 0; j < N; ++j)
+            for (int64_t t = 0; t < d; ++t)
+                Kh[j * d + t] *= jb->dk_blk[bh * jb->nblk + j / jb->blk_rows];
+    if (jb->dv_blk)
+        for (int64_t j = 0; j < N; ++j)
+            for (int64_t t = 0; t < d; ++t)
+#if ORACLE_MUTATION == 11
+                Vh[j * d + t] *= jb->dk_blk[bh * jb->nblk + j / jb->blk_rows]; /* planted */
+#else
+                Vh[j * d + t] *= jb->dv_blk[bh * jb->nblk + j / jb->blk_rows];
+#endif
 
     for (int64_t r = r_begin; r < r_end; ++r) {
         const int64_t i = jb->rows ? jb->rows[r] : r;
         load_elems(jb, jb->q, head_off + i * d, d, qrow);
+        if (jb->dq_blk) {
+#if ORACLE_MUTATION == 10
+            const double sq = jb->dq_blk[i / jb->blk_rows]; /* planted: head offset dropped */
+#else
+            const double sq = jb->dq_blk[bh * jb->nblk + i / jb->blk_rows];
+#endif
+            for (int64_t t = 0; t < d; ++t) qrow[t] *= sq;
+        }
 
         /* the keys this row may see */
         int64_t n_keys = N;
@@ -219,6 +243,40 @@ static void* worker(void* arg) {
     return NULL;
 }
 
+static int run_job(job_t* jb, int nthreads) {
+    jb->chunk = 64;
+    jb->n_items = jb->B * jb->H * ((jb->n_rows + jb->chunk - 1) / jb->chunk);
+    pthread_mutex_init(&jb->mu, NULL);
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > jb->n_items) nthreads = (int)jb->n_items;
+    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    if (!th) return -2;
+    int started = 0;
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&th[t], NULL, worker, jb) != 0) break;
+        ++started;
+    }
+    worker(jb);
+    for (int t = 1; t <= started; ++t) pthread_join(th[t], NULL);
+    free(th);
+    pthread_mutex_destroy(&jb->mu);
+    return jb->failed ? -2 : 0;
+}
+
+static int check_common(const void* q, const void* k, const void* v, int dtype, int64_t B,
+                        int64_t H, int64_t N, int64_t d, const int64_t* rows, int64_t* n_rows,
+                        const double* o, const double* lse) {
+    if (!q || !k || !v || !o || !lse) return -1;
+    if (B < 1 || H < 1 || N < 1 || d < 1) return -1;
+    if (dtype != OR_BF16 && dtype != OR_E4M3 && dtype != OR_F64) return -1;
+    if (!rows) *n_rows = N;
+    if (*n_rows < 1) return -1;
+    if (rows)
+        for (int64_t r = 0; r < *n_rows; ++r)
+            if (rows[r] < 0 || rows[r] >= N) return -1;
+    return 0;
+}
+
 /*
  * Evaluate O [B, H, n_rows, d] and LSE [B, H, n_rows] in fp64.
  *   q, k, v : [B, H, N, d] row-major operands (bf16 bits, e4m3 bits or fp64, per `dtype`)
@@ -230,16 +288,7 @@ int oracle_attention_fwd(const void* q, const void* k, const void* v, int dtype,
                          double descale_q, double descale_k, double descale_v,
                          const int64_t* rows, int64_t n_rows, double* o, double* lse,
                          int nthreads) {
-    if (!q || !k || !v || !o || !lse) return -1;
-    if (B < 1 || H < 1 || N < 1 || d < 1) return -1;
-    if (dtype != OR_BF16 && dtype != OR_E4M3 && dtype != OR_F64) return -1;
-    if (!rows) n_rows = N;
-    if (n_rows < 1) return -1;
-    if (rows)
-        for (int64_t r = 0; r < n_rows; ++r)
-            if (rows[r] < 0 || rows[r] >= N) return -1;
-    if (nthreads < 1) nthreads = 1;
-
+    if (check_common(q, k, v, dtype, B, H, N, d, rows, &n_rows, o, lse)) return -1;
     job_t jb;
     memset(&jb, 0, sizeof jb);
     jb.q = q;
@@ -259,23 +308,46 @@ int oracle_attention_fwd(const void* q, const void* k, const void* v, int dtype,
     jb.n_rows = n_rows;
     jb.o = o;
     jb.lse = lse;
-    jb.chunk = 64;
-    jb.n_items = B * H * ((n_rows + jb.chunk - 1) / jb.chunk);
-    pthread_mutex_init(&jb.mu, NULL);
+    return run_job(&jb, nthreads);
+}
 
-    if (nthreads > jb.n_items) nthreads = (int)jb.n_items;
-    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
-    if (!th) return -2;
-    int started = 0;
-    for (int t = 1; t < nthreads; ++t) {
-        if (pthread_create(&th[t], NULL, worker, &jb) != 0) break;
-        ++started;
-    }
-    worker(&jb);
-    for (int t = 1; t <= started; ++t) pthread_join(th[t], NULL);
-    free(th);
-    pthread_mutex_destroy(&jb.mu);
-    return jb.failed ? -2 : 0;
+/*
+ * Same evaluation with per-block descales: element (b, h, i, t) of Q has the value
+ * code * dq_blk[(b*H + h) * nblk + i / blk_rows], likewise K and V, nblk = ceil(N / blk_rows)
+ * (block quantisation, "FlashAttention · InkStack" section 3.3.1 and "FlashAttention 完全拆解
+ * （三）", block quantisation: each tile carries its own scale).
+ */
+int oracle_attention_fwd_blockscaled(const void* q, const void* k, const void* v, int dtype,
+                                     int64_t B, int64_t H, int64_t N, int64_t d, double scale,
+                                     int causal, const double* dq_blk, const double* dk_blk,
+                                     const double* dv_blk, int64_t blk_rows,
+                                     const int64_t* rows, int64_t n_rows, double* o,
+                                     double* lse, int nthreads) {
+    if (check_common(q, k, v, dtype, B, H, N, d, rows, &n_rows, o, lse)) return -1;
+    if (!dq_blk || !dk_blk || !dv_blk || blk_rows < 1) return -1;
+    job_t jb;
+    memset(&jb, 0, sizeof jb);
+    jb.q = q;
+    jb.k = k;
+    jb.v = v;
+    jb.dtype = dtype;
+    jb.B = B;
+    jb.H = H;
+    jb.N = N;
+    jb.d = d;
+    jb.scale = scale;
+    jb.causal = causal;
+    jb.dq = jb.dk = jb.dv = 1.0;
+    jb.dq_blk = dq_blk;
+    jb.dk_blk = dk_blk;
+    jb.dv_blk = dv_blk;
+    jb.blk_rows = blk_rows;
+    jb.nblk = (N + blk_rows - 1) / blk_rows;
+    jb.rows = rows;
+    jb.n_rows = n_rows;
+    jb.o = o;
+    jb.lse = lse;
+    return run_job(&jb, nthreads);
 }
 
 int oracle_mutation_id(void) { return ORACLE_MUTATION; }

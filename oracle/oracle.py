@@ -55,6 +55,13 @@ class Oracle:
                       ctypes.c_double, ctypes.c_int, ctypes.c_double, ctypes.c_double,
                       ctypes.c_double, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
                       ctypes.c_void_p, ctypes.c_int]
+        g = lib.oracle_attention_fwd_blockscaled
+        g.restype = ctypes.c_int
+        g.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                      ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                      ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                      ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
         lib.oracle_decode_bf16_array.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
         lib.oracle_decode_e4m3_array.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
         lib.oracle_mutation_id.restype = ctypes.c_int
@@ -75,13 +82,8 @@ class Oracle:
             raise ValueError(dtype)
         return out
 
-    def attention_fwd(self, q, k, v, scale: float, causal: bool = False, dtype: str = "f64",
-                      descale=(1.0, 1.0, 1.0), rows=None, threads: int | None = None):
-        """O [B,H,R,d] and LSE [B,H,R] in fp64 for the requested rows (all rows if None).
-
-        ``q``, ``k``, ``v`` are numpy arrays of shape [B,H,N,d]: float64 values for dtype
-        "f64", uint16 bf16 bit patterns for "bf16", uint8 e4m3 bit patterns for "e4m3".
-        """
+    @staticmethod
+    def _operands(q, k, v, dtype):
         q = np.ascontiguousarray(q)
         k = np.ascontiguousarray(k)
         v = np.ascontiguousarray(v)
@@ -91,12 +93,52 @@ class Oracle:
         for t in (q, k, v):
             if t.dtype != want:
                 raise TypeError(f"{dtype} operands must be {np.dtype(want).name}, got {t.dtype}")
-        B, H, N, d = q.shape
+        return q, k, v
+
+    @staticmethod
+    def _rows(rows, N):
         if rows is None:
-            R, rows_arr, rows_ptr = N, None, None
-        else:
-            rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
-            R, rows_ptr = rows_arr.size, rows_arr.ctypes.data
+            return N, None, None
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        return rows_arr.size, rows_arr, rows_arr.ctypes.data
+
+    def attention_fwd_blockscaled(self, q, k, v, scale: float, causal: bool, dtype: str,
+                                  dq_blk, dk_blk, dv_blk, blk_rows: int = 128, rows=None,
+                                  threads: int | None = None):
+        """Like ``attention_fwd`` with per-block descales: ``dq_blk`` etc. are [B,H,nblk]
+        arrays, nblk = ceil(N / blk_rows); row i of head (b, h) is scaled by
+        ``d*_blk[b, h, i // blk_rows]``."""
+        q, k, v = self._operands(q, k, v, dtype)
+        B, H, N, d = q.shape
+        nblk = -(-N // blk_rows)
+        scales = []
+        for s in (dq_blk, dk_blk, dv_blk):
+            s = np.ascontiguousarray(np.asarray(s, dtype=np.float64))
+            if s.shape != (B, H, nblk):
+                raise ValueError(f"block descales must be [B,H,{nblk}], got {s.shape}")
+            scales.append(s)
+        R, rows_arr, rows_ptr = self._rows(rows, N)
+        o = np.empty((B, H, R, d), dtype=np.float64)
+        lse = np.empty((B, H, R), dtype=np.float64)
+        rc = self._lib.oracle_attention_fwd_blockscaled(
+            q.ctypes.data, k.ctypes.data, v.ctypes.data, DTYPE_CODES[dtype], B, H, N, d,
+            float(scale), int(bool(causal)), scales[0].ctypes.data, scales[1].ctypes.data,
+            scales[2].ctypes.data, int(blk_rows), rows_ptr, R, o.ctypes.data, lse.ctypes.data,
+            int(threads or os.cpu_count() or 1))
+        if rc != 0:
+            raise RuntimeError(f"oracle_attention_fwd_blockscaled failed with code {rc}")
+        return o, lse
+
+    def attention_fwd(self, q, k, v, scale: float, causal: bool = False, dtype: str = "f64",
+                      descale=(1.0, 1.0, 1.0), rows=None, threads: int | None = None):
+        """O [B,H,R,d] and LSE [B,H,R] in fp64 for the requested rows (all rows if None).
+
+        ``q``, ``k``, ``v`` are numpy arrays of shape [B,H,N,d]: float64 values for dtype
+        "f64", uint16 bf16 bit patterns for "bf16", uint8 e4m3 bit patterns for "e4m3".
+        """
+        q, k, v = self._operands(q, k, v, dtype)
+        B, H, N, d = q.shape
+        R, rows_arr, rows_ptr = self._rows(rows, N)
         o = np.empty((B, H, R, d), dtype=np.float64)
         lse = np.empty((B, H, R), dtype=np.float64)
         if threads is None:

@@ -238,3 +238,51 @@ def pin_descaled_fp8_equals_f64_on_decoded_values(orc):
         o64, l64 = orc.attention_fwd(vals[0] * dq, vals[1] * dk, vals[2] * dv, 0.25, causal)
         np.testing.assert_allclose(o8, o64, rtol=1e-12, atol=1e-12)
         np.testing.assert_allclose(l8, l64, rtol=1e-12, atol=1e-12)
+
+
+def _e4m3_values(raw):
+    return torch.from_numpy(raw.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def _random_codes(rng, shape):
+    raw = rng.integers(0, 256, size=shape, dtype=np.uint8)
+    raw[(raw & 0x7F) == 0x7F] = 0x38  # no NaN codes
+    return raw
+
+
+@pin
+def pin_block_descales_equal_f64_on_expanded_values(orc):
+    """Per-block descales (one per 16-row block of each head, all different) give the f64
+    result on code value x the descale of the row's block, the expansion done here with
+    numpy's repeat ("FlashAttention · InkStack", section 3.3.1 "Block Quantization")."""
+    rng = np.random.default_rng(21)
+    B, H, N, d, blk = 2, 2, 37, 8, 16
+    nblk = -(-N // blk)
+    raw = _random_codes(rng, (3, B, H, N, d))
+    vals = _e4m3_values(raw)
+    sc = np.exp2(rng.uniform(-7, -3, size=(3, B, H, nblk)))
+    full = [vals[t] * np.repeat(sc[t], blk, axis=2)[:, :, :N, None] for t in range(3)]
+    for causal in (False, True):
+        ob, lb = orc.attention_fwd_blockscaled(raw[0], raw[1], raw[2], 0.5, causal, "e4m3",
+                                               sc[0], sc[1], sc[2], blk)
+        o64, l64 = orc.attention_fwd(full[0], full[1], full[2], 0.5, causal)
+        np.testing.assert_allclose(ob, o64, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lb, l64, rtol=1e-12, atol=1e-12)
+
+
+@pin
+def pin_uniform_block_descales_equal_per_tensor(orc):
+    """Block descales that are all equal reduce to the per-tensor descaled result
+    ("FlashAttention · InkStack", section 3.3.3 "Scaling")."""
+    rng = np.random.default_rng(22)
+    B, H, N, d = 1, 3, 40, 16
+    raw = _random_codes(rng, (3, B, H, N, d))
+    dq, dk, dv = 0.011, 0.017, 0.023
+    for blk in (8, 128):
+        nblk = -(-N // blk)
+        s = [np.full((B, H, nblk), x) for x in (dq, dk, dv)]
+        ob, lb = orc.attention_fwd_blockscaled(raw[0], raw[1], raw[2], 0.3, True, "e4m3",
+                                               *s, blk)
+        ot, lt = orc.attention_fwd(raw[0], raw[1], raw[2], 0.3, True, "e4m3", (dq, dk, dv))
+        np.testing.assert_allclose(ob, ot, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lb, lt, rtol=1e-12, atol=1e-12)

@@ -3,7 +3,7 @@
 The oracle's C source carries a handful of deliberate mistakes behind ``ORACLE_MUTATION``
 (a dropped scale, an off-by-one causal mask, a dropped max in the LSE, the wrong operand in P.V,
 a dropped normalisation, a shifted value index, an ignored value descale, a wrong e4m3 exponent
-bias, a base-2 LSE).  The default build has none.
+bias, a base-2 LSE, two block-descale indexing slips).  The default build has none.
 """
 import os
 
@@ -22,6 +22,8 @@ MUTATIONS = {
     7: "value descale ignored",
     8: "e4m3 exponent bias 8",
     9: "LSE in base 2",
+    10: "query block descale read from the first head",
+    11: "key block descale applied to the values",
 }
 
 

@@ -138,6 +138,58 @@ def random_inputs(B: int, H: int, N: int, d: int, dtype: str = "bf16", seed: int
     raise ValueError(f"unknown operand dtype {dtype!r}")
 
 
+def outlier_inputs(B: int, H: int, N: int, d: int, seed: int = 0) -> Inputs:
+    """Q, K, V with heavy-tailed entries N(0,1) + N(0,100)·Bernoulli(0.001), the outlier
+    distribution of the pages' fp8 accuracy study ("FlashAttention 完全拆解（三）", section
+    "数值误差验证"), drawn in fp32 (Q, then K, then V; per tensor: normal part, outlier part,
+    Bernoulli mask) and rounded to bf16."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    shape = (B, H, N, d)
+    out = []
+    for _ in range(3):
+        base = torch.randn(shape, generator=g, dtype=torch.float32)
+        big = torch.randn(shape, generator=g, dtype=torch.float32) * 10.0
+        mask = torch.rand(shape, generator=g, dtype=torch.float32) < 0.001
+        out.append((base + big * mask).to(torch.bfloat16))
+    return Inputs(*out)
+
+
+def hadamard_signs(d: int, seed: int) -> torch.Tensor:
+    """A seeded random +-1 vector of length d (fp32), the diagonal of the incoherent transform."""
+    g = torch.Generator(device="cpu").manual_seed(seed + 4242)
+    return (torch.randint(0, 2, (d,), generator=g) * 2 - 1).to(torch.float32)
+
+
+@dataclass
+class BlockScaledInputs:
+    """e4m3 codes with one fp32 descale per 128-row block of each head ([B, H, nblk])."""
+
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    dq: torch.Tensor
+    dk: torch.Tensor
+    dv: torch.Tensor
+
+    def raw(self, name: str):
+        return getattr(self, name).contiguous().view(torch.uint8).numpy()
+
+
+def blockscaled_inputs(B: int, H: int, N: int, d: int, seed: int = 0,
+                       spread_log2: float = 1.5) -> BlockScaledInputs:
+    """Random operands for the block-scaled fp8 path: the per-tensor e4m3 codes of
+    ``random_inputs`` and, for every 128-row block, a descale equal to the per-tensor one times
+    2^u with u uniform in [-spread_log2, spread_log2] (seeded; Q, K, V in that order)."""
+    base = random_inputs(B, H, N, d, "e4m3", seed)
+    g = torch.Generator(device="cpu").manual_seed(seed + 9191)
+    nblk = -(-N // 128)
+    ds = []
+    for d0 in (base.descale_q, base.descale_k, base.descale_v):
+        u = (torch.rand((B, H, nblk), generator=g, dtype=torch.float64) * 2 - 1) * spread_log2
+        ds.append((d0 * torch.exp2(u)).to(torch.float32))
+    return BlockScaledInputs(base.q, base.k, base.v, *ds)
+
+
 def make_inputs(w: Workload) -> Inputs:
     return random_inputs(w.B, w.H, w.N, w.d, w.dtype, w.seed, w.q_mult)
 
