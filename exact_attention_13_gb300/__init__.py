@@ -24,6 +24,7 @@ FA_ERR_UNSUPPORTED = 2
 FA_ERR_MISALIGNED = 3
 FA_ERR_CUDA = 4
 FA_ERR_DEVICE_TIMEOUT = 5
+FA_QUANT_POW2_DESCALE = 1
 FA_DTYPE_BF16 = 0
 FA_DTYPE_FP8_E4M3 = 1
 
@@ -48,6 +49,13 @@ SIGNATURES = {
                                         _c.c_void_p, _c.c_int, _c.c_int, _c.c_int, _c.c_int,
                                         _c.c_float, _c.c_int, _c.c_int, _c.c_int, _c.c_void_p,
                                         _c.c_void_p]),
+    "fa_fwd_fp8_blockscaled": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                                          _c.c_void_p, _c.c_int, _c.c_int, _c.c_int, _c.c_int,
+                                          _c.c_float, _c.c_int, _c.c_void_p, _c.c_void_p,
+                                          _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_size_t,
+                                          _c.c_void_p, _c.c_void_p]),
+    "fa_quantize_e4m3": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_int,
+                                    _c.c_int, _c.c_int, _c.c_void_p, _c.c_int, _c.c_void_p]),
     "fa_device_status": (_c.c_int, [_c.c_int, _c.POINTER(_c.c_int)]),
     "fa_status_string": (_c.c_char_p, [_c.c_int]),
     "fa_version": (_c.c_int, []),
@@ -138,6 +146,21 @@ def fa_fwd_split_noalloc(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, scale,
                                       stream)
 
 
+def fa_fwd_fp8_blockscaled(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, scale, causal,
+                           dq_blk_ptr, dk_blk_ptr, dv_blk_ptr, num_splits=1, workspace_ptr=None,
+                           workspace_bytes=0, status_ptr=None, stream=None) -> int:
+    return lib().fa_fwd_fp8_blockscaled(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, scale,
+                                        int(causal), dq_blk_ptr, dk_blk_ptr, dv_blk_ptr,
+                                        int(num_splits), workspace_ptr, int(workspace_bytes),
+                                        status_ptr, stream)
+
+
+def fa_quantize_e4m3(x_ptr, codes_ptr, descales_ptr, B, H, N, d, signs_ptr=None, flags=0,
+                     stream=None) -> int:
+    return lib().fa_quantize_e4m3(x_ptr, codes_ptr, descales_ptr, B, H, N, d, signs_ptr,
+                                  int(flags), stream)
+
+
 def split_workspace_bytes(B: int, H: int, N: int, d: int, num_splits: int) -> int:
     return int(lib().fa_fwd_split_workspace_bytes(B, H, N, d, num_splits))
 
@@ -210,6 +233,86 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, descale=None,
                           lse.data_ptr(), B, H, N, d, float(scale), causal, dtype, num_splits,
                           workspace.data_ptr(), nbytes, (dq, dk, dv), st, stream)
     _check(rc, "fa_fwd_split")
+    return out, lse
+
+
+def quantize_e4m3(x, signs=None, pow2: bool = False, codes=None, descales=None):
+    """Block-quantise a bf16 CUDA tensor [B, H, N, d] to e4m3 (one fp32 descale per 128-row
+    block of each head), first applying the incoherent transform diag(signs) Had / sqrt(d) to
+    every row when ``signs`` (a CUDA fp32 tensor of d values +-1) is given; ``pow2`` rounds the
+    descales up to powers of two (use it for V).  Returns (codes float8_e4m3fn [B, H, N, d],
+    descales fp32 [B, H, ceil(N / 128)])."""
+    import torch
+
+    if not x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != 4 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous bf16 CUDA tensor [B, H, N, d]")
+    B, H, N, d = x.shape
+    nblk = -(-N // 128)
+    if codes is None:
+        codes = torch.empty((B, H, N, d), dtype=torch.float8_e4m3fn, device=x.device)
+    if descales is None:
+        descales = torch.empty((B, H, nblk), dtype=torch.float32, device=x.device)
+    if codes.shape != x.shape or codes.dtype != torch.float8_e4m3fn or not codes.is_contiguous():
+        raise ValueError("codes must be a contiguous float8_e4m3fn tensor shaped like x")
+    if descales.shape != (B, H, nblk) or descales.dtype != torch.float32:
+        raise ValueError(f"descales must be fp32 [B, H, {nblk}]")
+    sp = None
+    if signs is not None:
+        if signs.shape != (d,) or signs.dtype != torch.float32 or not signs.is_cuda:
+            raise ValueError("signs must be a CUDA fp32 tensor of d values")
+        sp = signs.data_ptr()
+    stream = torch.cuda.current_stream(x.device).cuda_stream
+    with torch.cuda.device(x.device):
+        rc = fa_quantize_e4m3(x.data_ptr(), codes.data_ptr(), descales.data_ptr(), B, H, N, d,
+                              sp, FA_QUANT_POW2_DESCALE if pow2 else 0, stream)
+    _check(rc, "fa_quantize_e4m3")
+    return codes, descales
+
+
+def fwd_fp8_blockscaled(q, k, v, dq_blk, dk_blk, dv_blk, causal: bool = False,
+                        scale: float | None = None, out=None, lse=None, status=None,
+                        num_splits: int = 1, workspace=None):
+    """Attention forward on float8_e4m3fn CUDA tensors with per-block descales
+    (fp32 [B, H, ceil(N / 128)] each, as ``quantize_e4m3`` returns); returns (o bf16, lse)."""
+    import torch
+
+    for t in (q, k, v):
+        if not t.is_cuda or t.dtype != torch.float8_e4m3fn or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous float8_e4m3fn CUDA tensors")
+    if q.shape != k.shape or q.shape != v.shape or q.dim() != 4:
+        raise ValueError("q, k, v must share one [B, H, N, d] shape")
+    B, H, N, d = q.shape
+    nblk = -(-N // 128)
+    for t in (dq_blk, dk_blk, dv_blk):
+        if (t.shape != (B, H, nblk) or t.dtype != torch.float32 or not t.is_cuda
+                or not t.is_contiguous()):
+            raise ValueError(f"block descales must be contiguous fp32 CUDA [B, H, {nblk}]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
+    ws_ptr, ws_bytes = None, 0
+    if num_splits > 1:
+        need = split_workspace_bytes(B, H, N, d, num_splits)
+        if need == 0:
+            raise ValueError(f"invalid split configuration (num_splits={num_splits}, d={d})")
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    st = status.data_ptr() if status is not None else None
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    with torch.cuda.device(q.device):
+        rc = fa_fwd_fp8_blockscaled(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                    lse.data_ptr(), B, H, N, d, float(scale), causal,
+                                    dq_blk.data_ptr(), dk_blk.data_ptr(), dv_blk.data_ptr(),
+                                    num_splits, ws_ptr, ws_bytes, st, stream)
+    _check(rc, "fa_fwd_fp8_blockscaled")
     return out, lse
 
 

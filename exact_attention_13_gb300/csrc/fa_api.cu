@@ -10,6 +10,7 @@
 
 #include "../../include/exact_attention.h"
 #include "fa_fwd_kernel.cuh"
+#include "fa_quant.cuh"
 
 namespace exattn {
 namespace {
@@ -81,10 +82,17 @@ bool encode_operand_map(CUtensorMap* map, const void* ptr, int elem_bytes, int d
   return r == CUDA_SUCCESS;
 }
 
+// Per-block fp8 descales, [B*H, ceil(N / 128)] each (null: per-tensor descales).
+struct BlockScales {
+  const float* dq;
+  const float* dk;
+  const float* dv;
+};
+
 template <int D, bool FP8, bool CAUSAL>
 int launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
            float c, float out_mult, int* status, int splits, float* o_part, float* lse_part,
-           cudaStream_t stream) {
+           const BlockScales* bs, cudaStream_t stream) {
   constexpr int elem = FP8 ? 1 : 2;
   CUtensorMap mq, mk, mv;
   const int bh = B * H;
@@ -115,6 +123,10 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   args.bh = bh;
   args.c = c;
   args.out_mult = out_mult;
+  args.dq_blk = bs ? bs->dq : nullptr;
+  args.dk_blk = bs ? bs->dk : nullptr;
+  args.dv_blk = bs ? bs->dv : nullptr;
+  args.nblk = (N + kTileRows - 1) / kTileRows;
   const unsigned mblocks = static_cast<unsigned>((N + kCtaRows - 1) / kCtaRows);
   const unsigned z = static_cast<unsigned>(splits);
   const dim3 grid = CAUSAL ? dim3(static_cast<unsigned>(bh), mblocks, z)
@@ -126,9 +138,10 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
 template <int D, bool FP8>
 int launch_mask(int causal, const void* q, const void* k, const void* v, void* o, float* lse,
                 int B, int H, int N, float c, float om, int* st, int splits, float* op,
-                float* lp, cudaStream_t s) {
-  return causal ? launch<D, FP8, true>(q, k, v, o, lse, B, H, N, c, om, st, splits, op, lp, s)
-                : launch<D, FP8, false>(q, k, v, o, lse, B, H, N, c, om, st, splits, op, lp, s);
+                float* lp, const BlockScales* bs, cudaStream_t s) {
+  return causal
+             ? launch<D, FP8, true>(q, k, v, o, lse, B, H, N, c, om, st, splits, op, lp, bs, s)
+             : launch<D, FP8, false>(q, k, v, o, lse, B, H, N, c, om, st, splits, op, lp, bs, s);
 }
 
 // Merge of key splits ("FlashAttention · InkStack", section 2.2: key blocks can be processed
@@ -194,11 +207,13 @@ __global__ void exp2_probe_kernel(const float* x, float* y, long long n, int mod
 namespace exattn {
 namespace {
 
-// Shared argument checks and dispatch of fa_fwd_ex / fa_fwd_split.  splits == 1 writes O and
-// LSE directly; splits > 1 writes per-split partials into `workspace`, then merges them.
+// Shared argument checks and dispatch of fa_fwd_ex / fa_fwd_split / fa_fwd_fp8_blockscaled.
+// splits == 1 writes O and LSE directly; splits > 1 writes per-split partials into
+// `workspace`, then merges them.  `bs` (fp8 only) replaces the per-tensor descales.
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
              int N, int d, float scale, int causal, int dtype, const fa_fwd_opts* opts,
-             int splits, void* workspace, size_t workspace_bytes, void* stream) {
+             int splits, void* workspace, size_t workspace_bytes, void* stream,
+             const BlockScales* bs = nullptr) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
   if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP8_E4M3) return FA_ERR_INVALID_ARG;
@@ -230,6 +245,11 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     o_part = static_cast<float*>(workspace);
     lse_part = o_part + static_cast<size_t>(splits) * B * H * N * d;
   }
+  if (bs) {
+    if (dtype != FA_DTYPE_FP8_E4M3 || !bs->dq || !bs->dk || !bs->dv) return FA_ERR_INVALID_ARG;
+    if (!aligned(bs->dq, 4) || !aligned(bs->dk, 4) || !aligned(bs->dv, 4))
+      return FA_ERR_MISALIGNED;
+  }
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
       !aligned(lse, 4) || (status && !aligned(status, 4)))
     return FA_ERR_MISALIGNED;
@@ -240,14 +260,14 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   int rc;
   if (dtype == FA_DTYPE_BF16) {
     rc = d == 64 ? launch_mask<64, false>(causal, q, k, v, o, lse, B, H, N, cf, 1.f, status,
-                                          splits, o_part, lse_part, s)
+                                          splits, o_part, lse_part, nullptr, s)
                  : launch_mask<128, false>(causal, q, k, v, o, lse, B, H, N, cf, 1.f, status,
-                                           splits, o_part, lse_part, s);
+                                           splits, o_part, lse_part, nullptr, s);
   } else {
     rc = d == 64 ? launch_mask<64, true>(causal, q, k, v, o, lse, B, H, N, cf, dv, status,
-                                         splits, o_part, lse_part, s)
+                                         splits, o_part, lse_part, bs, s)
                  : launch_mask<128, true>(causal, q, k, v, o, lse, B, H, N, cf, dv, status,
-                                          splits, o_part, lse_part, s);
+                                          splits, o_part, lse_part, bs, s);
   }
   if (rc != FA_OK || splits == 1) return rc;
   const long long rows = static_cast<long long>(B) * H * N;
@@ -282,6 +302,48 @@ int fa_fwd_split(const void* q, const void* k, const void* v, void* o, float* ls
                  void* stream) {
   return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, opts, num_splits,
                   workspace, workspace_bytes, stream);
+}
+
+int fa_fwd_fp8_blockscaled(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int H, int N, int d, float scale, int causal,
+                           const float* descale_q_blk, const float* descale_k_blk,
+                           const float* descale_v_blk, int num_splits, void* workspace,
+                           size_t workspace_bytes, int* dev_status, void* stream) {
+  fa_fwd_opts opts;
+  opts.descale_q = opts.descale_k = opts.descale_v = 1.f;
+  opts.dev_status = dev_status;
+  const BlockScales bs{descale_q_blk, descale_k_blk, descale_v_blk};
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, FA_DTYPE_FP8_E4M3, &opts,
+                  num_splits, workspace, workspace_bytes, stream, &bs);
+}
+
+int fa_quantize_e4m3(const void* x, void* codes, float* descales, int B, int H, int N, int d,
+                     const float* signs, int flags, void* stream) {
+  if (!x || !codes || !descales || B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (flags & ~FA_QUANT_POW2_DESCALE) return FA_ERR_INVALID_ARG;
+  const bool pow2 = (flags & FA_QUANT_POW2_DESCALE) != 0;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H > 65535) return FA_ERR_UNSUPPORTED;
+  if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(descales, 4) ||
+      (signs && !aligned(signs, 16)))
+    return FA_ERR_MISALIGNED;
+  const int nblk = (N + kQuantRows - 1) / kQuantRows;
+  const dim3 grid(static_cast<unsigned>(nblk), static_cast<unsigned>(B * H));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const auto* xb = static_cast<const __nv_bfloat16*>(x);
+  auto* cb = static_cast<uint8_t*>(codes);
+  if (d == 64) {
+    if (signs)
+      quantize_e4m3_kernel<64, true><<<grid, kQuantThreads, 0, s>>>(xb, cb, descales, signs, N, nblk, pow2);
+    else
+      quantize_e4m3_kernel<64, false><<<grid, kQuantThreads, 0, s>>>(xb, cb, descales, signs, N, nblk, pow2);
+  } else {
+    if (signs)
+      quantize_e4m3_kernel<128, true><<<grid, kQuantThreads, 0, s>>>(xb, cb, descales, signs, N, nblk, pow2);
+    else
+      quantize_e4m3_kernel<128, false><<<grid, kQuantThreads, 0, s>>>(xb, cb, descales, signs, N, nblk, pow2);
+  }
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,

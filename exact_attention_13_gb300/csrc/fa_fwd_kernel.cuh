@@ -134,7 +134,21 @@ struct KernelArgs {
   int bh;             // batch * heads
   float c;            // scale * log2(e) * descale_q * descale_k
   float out_mult;     // descale_v (1 for bf16)
+  // fp8 block scaling (null for per-tensor descales): one fp32 descale per 128-row block of
+  // each head, [BH, nblk]; c and out_mult then carry no descale of their own
+  const float* dq_blk;
+  const float* dk_blk;
+  const float* dv_blk;
+  int nblk;
 };
+
+// e4m3 probabilities are stored as 2^kPOffsetLog2 * p: the largest is 256 (< 448, the format's
+// largest finite value) and p down to 2^-14 stays out of the subnormal range.  O and l carry
+// the same factor, so it cancels in O / l; the LSE takes it back out.
+template <bool FP8>
+__host__ __device__ constexpr float p_offset_log2() {
+  return FP8 ? 8.f : 0.f;
+}
 
 // Compile-time geometry of one instance.
 template <int D, bool FP8>
@@ -493,12 +507,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(w4 * 32) << 16;
     const uint32_t t_s = tmem + lane_addr + h * 128;        // S_h / P_h
     const uint32_t t_o = tmem + lane_addr + 256 + h * 128;  // O_h
-    const float c = args.c;
+    float c = args.c;
     float m_run = -INFINITY;  // running max of scaled logits, log2 units
-    float l_run = 0.f;        // running sum of 2^(x - m_run)
+    float l_run = 0.f;        // running sum of 2^(x - m_run) (times 2^p_offset_log2)
     bool ok = true;
+    // fp8 block scaling ("FlashAttention · InkStack", section 3.3.1 "Block Quantization"): the
+    // score block (i, j) is scaled by dq_i dk_j, folded into the exponent's multiplier; the value
+    // block's dv_j is folded into P as the factor dv_j / dv_max <= 1 (a shift of the exponent),
+    // l takes the inverse factor and the output multiplier is dv_max.  With power-of-two value
+    // descales the fold is exact; otherwise the factor shares P's e4m3 rounding.
+    const bool blockscaled = FP8 && args.dk_blk != nullptr;
+    const size_t blk_base = static_cast<size_t>(bh) * args.nblk;
+    float dv_max = 1.f;
+    if (blockscaled) {
+      float mx = 0.f;
+      for (int t = lane; t < args.nblk; t += 32) mx = fmaxf(mx, __ldg(args.dv_blk + blk_base + t));
+#pragma unroll
+      for (int off = 16; off >= 1; off /= 2) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      dv_max = mx;
+      const int qblk = mblock * 2 + h;
+      if (qblk < args.nblk) c *= __ldg(args.dq_blk + blk_base + qblk);
+    }
 
     for (int j = 0; j < nkv_h; ++j) {
+      float c_j = c;                             // multiplier of this key block's raw scores
+      float bias_j = p_offset_log2<FP8>();       // added to every exponent of the block
+      float l_mult = 1.f;                        // l gathers rowsum * l_mult
+      if (blockscaled) {
+        const float dk = __ldg(args.dk_blk + blk_base + jb + j);
+        const float dv = __ldg(args.dv_blk + blk_base + jb + j);
+        c_j = c * dk;
+        // log2(dv / dv_max) as exponent + log2(mantissa): exact when the ratio is a power of
+        // two, so P then carries no rounding beyond its own e4m3 rounding
+        const uint32_t rb = __float_as_uint(dv / dv_max);
+        const float mant = __uint_as_float((rb & 0x007FFFFFu) | 0x3F800000u);
+        bias_j += static_cast<float>(static_cast<int>((rb >> 23) & 0xFFu) - 127) +
+                  (mant == 1.f ? 0.f : lg2_mufu(mant));
+        l_mult = dv_max / dv;
+      }
       ok = wait_phase(smem_u32(&ctl->s_full[h]), j & 1, abort_flag, args.status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -540,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int w = 4; w >= 1; w /= 2)
 #pragma unroll
         for (int k = 0; k < w; ++k) mp[k] = fmaxf(mp[k], mp[k + w]);
-      const float m_cand = fmaxf(m_run, mp[0] * c);
+      const float m_cand = fmaxf(m_run, mp[0] * c_j);
       if (threadIdx.x % 128 == 0) EXATTN_TRACE_EVENT(1, h, j);
 
       // Rescale O and l when some row of the warp grew its max by more than kRescaleLog2 (the
@@ -568,12 +614,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // test lives in its own instantiation so unmasked blocks run a select-free loop
       const uint32_t pb0 = smem_u32(&ctl->p_full[h][0]);
       const uint32_t pb1 = smem_u32(&ctl->p_full[h][kPHalves == 2 ? 1 : 0]);
+      const float m_shift = m_run - bias_j;
       const float rowsum =
-          masked ? exp_and_publish<true, FP8, kPHalves, 0>(s, c, m_run, lim, t_s, pb0, pb1, lane)
-                 : exp_and_publish<false, FP8, kPHalves, EXATTN_EMU_EVERY>(s, c, m_run, lim, t_s,
-                                                                           pb0, pb1, lane);
+          masked ? exp_and_publish<true, FP8, kPHalves, 0>(s, c_j, m_shift, lim, t_s, pb0, pb1,
+                                                           lane)
+                 : exp_and_publish<false, FP8, kPHalves, EXATTN_EMU_EVERY>(s, c_j, m_shift, lim,
+                                                                           t_s, pb0, pb1, lane);
       if (threadIdx.x % 128 == 0) EXATTN_TRACE_EVENT(3, h, j);
-      l_run += rowsum;
+      l_run = fmaf(rowsum, l_mult, l_run);
     }
 
     if (ok && nkv_h > 0) {
@@ -581,9 +629,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();
-        const float inv_l = args.out_mult / l_run;
+        const float inv_l = (blockscaled ? dv_max : args.out_mult) / l_run;
         const bool live = row < n;
-        const float lse_row = (m_run + lg2_mufu(l_run)) * kLn2;
+        const float lse_row = (m_run + lg2_mufu(l_run) - p_offset_log2<FP8>()) * kLn2;
         if (nsplit == 1) {
           __nv_bfloat16* orow = args.o + (static_cast<size_t>(bh) * n + (live ? row : 0)) * D;
 #pragma unroll

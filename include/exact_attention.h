@@ -144,6 +144,56 @@ FA_API int fa_fwd_split_noalloc(const void* q, const void* k, const void* v, voi
                                 void* stream);
 
 /*
+ * fp8 forward with block scaling ("FlashAttention · InkStack", section 3.3.1 "Block
+ * Quantization"; "FlashAttention 完全拆解（三）", section on block quantisation): every block of
+ * 128 consecutive rows of one head of Q, K and V carries its own descale, so the stored value of
+ * row i of head (b, h) is code * descale_X_blk[(b * H + h) * nblk + i / 128], nblk = ceil(N / 128).
+ * Score block (i, j) is then scale * dq_i * dk_j * (q . k) and the output sum_j P_ij dv_j V_j.
+ *   q, k, v           : device pointers, [B, H, N, d] e4m3fn codes (16-byte aligned)
+ *   descale_*_blk     : device pointers, [B, H, nblk] fp32 (4-byte aligned); every descale must
+ *                       be finite and > 0 (fa_quantize_e4m3 writes such arrays), otherwise the
+ *                       output is undefined (the kernel still runs to completion).  The value
+ *                       descales enter P as dv_j / max_j dv_j: exact for powers of two, else
+ *                       rounded with P (see FA_QUANT_POW2_DESCALE)
+ *   num_splits, workspace, workspace_bytes : as fa_fwd_split (1 and NULL, 0 for no key split)
+ *   dev_status        : as fa_fwd_opts.dev_status (NULL = the library's status word)
+ * Other arguments, layouts and errors as fa_fwd_split.
+ */
+FA_API int fa_fwd_fp8_blockscaled(const void* q, const void* k, const void* v, void* o,
+                                  float* lse, int B, int H, int N, int d, float scale,
+                                  int causal, const float* descale_q_blk,
+                                  const float* descale_k_blk, const float* descale_v_blk,
+                                  int num_splits, void* workspace, size_t workspace_bytes,
+                                  int* dev_status, void* stream);
+
+/* fa_quantize_e4m3 flag: round every descale up to a power of two (recommended for V). */
+#define FA_QUANT_POW2_DESCALE 1
+
+/*
+ * Block quantiser to fp8 e4m3fn, with optional incoherent processing ("FlashAttention ·
+ * InkStack", sections 3.3.1 "Block Quantization", 3.3.2 "Incoherent Processing" and 3.3.3
+ * "Scaling").  For every block of 128 consecutive rows of each head:
+ *     X'        = X diag(signs) Had / sqrt(d)   if signs != NULL (fast Walsh-Hadamard transform;
+ *                 Had is the Sylvester-Hadamard matrix), else X' = X
+ *     descale   = max |X'_blk| / 448            (1 if the block is all zero); with
+ *                 FA_QUANT_POW2_DESCALE, the smallest power of two >= that quotient
+ *     code      = e4m3(X' / descale)            (round to nearest even, saturate at 448)
+ * Apply the same `signs` to Q and K (QK^T is unchanged) and none to V.  Power-of-two value
+ * descales let fa_fwd_fp8_blockscaled fold them into P exactly; other value descales add one
+ * more e4m3 rounding of relative size up to 2^-4 to each probability.
+ *   x        : device pointer, [B, H, N, d] bf16 (16-byte aligned)
+ *   codes    : device pointer, [B, H, N, d] e4m3fn output (16-byte aligned)
+ *   descales : device pointer, [B, H, ceil(N / 128)] fp32 output (4-byte aligned)
+ *   signs    : device pointer to d fp32 values, each +1 or -1 (16-byte aligned), or NULL
+ *   d        : 64 or 128; B * H <= 65535
+ *   flags    : 0 or FA_QUANT_POW2_DESCALE (other bits: FA_ERR_INVALID_ARG)
+ * Arithmetic is fp32 (correctly rounded quotients).  Returns an fa_status; asynchronous on
+ * `stream` like fa_fwd.
+ */
+FA_API int fa_quantize_e4m3(const void* x, void* codes, float* descales, int B, int H, int N,
+                            int d, const float* signs, int flags, void* stream);
+
+/*
  * Read, and if `clear` is nonzero reset to FA_OK, the library's status word on the current
  * device.  Synchronises the device first.  Writes FA_OK or FA_ERR_DEVICE_TIMEOUT to *out.
  * Returns an fa_status for the call itself.

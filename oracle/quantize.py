@@ -21,6 +21,8 @@ What it computes (pages cited by title and section):
 
 Readings where the pages leave a step open: the block is the attention kernel's 128-row tile;
 one sign vector s serves every head; the quotient is x / descale, not x times a reciprocal.
+Optionally (``pow2``) the descale is raised to the next power of two, a choice of this library
+for value blocks (e4m3's relative precision does not depend on the scale).
 """
 from __future__ import annotations
 
@@ -80,9 +82,9 @@ def round_to_e4m3(y: np.ndarray):
     return code, val
 
 
-def block_quantize(x: np.ndarray, blk_rows: int = 128, signs=None):
+def block_quantize(x: np.ndarray, blk_rows: int = 128, signs=None, pow2: bool = False):
     """Quantise X [B, H, N, d] block-wise; returns (codes uint8 [B,H,N,d], descales fp32
-    [B,H,nblk], scaled fp64 [B,H,N,d]).
+    [B,H,nblk], scaled fp64 [B,H,N,d]).  ``pow2`` rounds each descale up to a power of two.
 
     ``scaled`` is the fp64 value of (transformed fp32 value) / (fp32 descale) before rounding,
     for tests that have to tell rounding ties apart from errors.
@@ -101,6 +103,8 @@ def block_quantize(x: np.ndarray, blk_rows: int = 128, signs=None):
         blk = x32[:, :, j * blk_rows:(j + 1) * blk_rows]
         amax = np.abs(blk).max(axis=(2, 3))
         ds = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+        if pow2:
+            ds = np.exp2(np.ceil(np.log2(ds.astype(np.float64)))).astype(np.float32)
         descales[:, :, j] = ds
         y = (blk / ds[:, :, None, None]).astype(np.float32)
         codes[:, :, j * blk_rows:(j + 1) * blk_rows] = round_to_e4m3(y)[0]

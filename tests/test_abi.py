@@ -97,3 +97,39 @@ def test_split_host_checks(lib, splits, ws, nbytes, want):
     rc = ea.fa_fwd_split(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 128, 0.1, 0, 0, splits,
                          ws, nbytes, (1.0, 1.0, 1.0), None, None)
     assert rc == want
+
+
+@pytest.mark.parametrize("blk,want", [
+    ((0, FAKE, FAKE), ea.FA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, 0), ea.FA_ERR_INVALID_ARG),
+    ((FAKE, FAKE + 2, FAKE), ea.FA_ERR_MISALIGNED),
+])
+def test_blockscaled_host_checks(lib, blk, want):
+    rc = ea.fa_fwd_fp8_blockscaled(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 128, 0.1, 0, *blk)
+    assert rc == want
+
+
+def test_blockscaled_shares_the_shape_checks(lib):
+    assert ea.fa_fwd_fp8_blockscaled(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 96, 0.1, 0, FAKE,
+                                     FAKE, FAKE) == ea.FA_ERR_UNSUPPORTED
+    assert ea.fa_fwd_fp8_blockscaled(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 128, 0.1, 0, FAKE,
+                                     FAKE, FAKE, 2, 0, 0) == ea.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("args,want", [
+    ((0, FAKE, FAKE, 1, 1, 128, 128, None), ea.FA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, 0, 1, 1, 128, 128, None), ea.FA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, 1, 0, 128, 128, None), ea.FA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, 1, 1, 128, 32, None), ea.FA_ERR_UNSUPPORTED),
+    ((FAKE, FAKE, FAKE, 256, 256, 128, 128, None), ea.FA_ERR_UNSUPPORTED),
+    ((FAKE + 8, FAKE, FAKE, 1, 1, 128, 128, None), ea.FA_ERR_MISALIGNED),
+    ((FAKE, FAKE, FAKE + 1, 1, 1, 128, 128, None), ea.FA_ERR_MISALIGNED),
+    ((FAKE, FAKE, FAKE, 1, 1, 128, 128, FAKE + 4), ea.FA_ERR_MISALIGNED),
+])
+def test_quantize_host_checks(lib, args, want):
+    assert ea.fa_quantize_e4m3(*args, 0, None) == want
+
+
+def test_quantize_rejects_unknown_flags(lib):
+    assert ea.fa_quantize_e4m3(FAKE, FAKE, FAKE, 1, 1, 128, 128, None, 2, None) == \
+        ea.FA_ERR_INVALID_ARG

@@ -131,3 +131,22 @@ def test_block_quantize_scales_and_error_bound(signs):
     err = np.abs(rec - xt)
     assert np.all(err <= np.abs(xt) * 2.0 ** -4 + np.repeat(descales, 128, axis=2)[:, :, :N, None]
                   * 2.0 ** -10)
+
+
+def test_power_of_two_descales():
+    """With ``pow2`` each descale is the smallest power of two at or above amax / 448, so the
+    block's largest code lies in (224, 448] and x / descale is exact before the e4m3 rounding."""
+    rng = np.random.default_rng(35)
+    x = (rng.standard_normal((1, 2, 260, 64)) * rng.uniform(0.01, 50, (1, 2, 1, 1)))
+    x = x.astype(np.float32)
+    c1, d1, _ = qz.block_quantize(x, 128)
+    c2, d2, scaled = qz.block_quantize(x, 128, pow2=True)
+    m, e = np.frexp(d2.astype(np.float64))
+    assert np.all(m == 0.5)
+    assert np.all(d2 >= d1) and np.all(d2 < 2 * d1)
+    vals = torch.from_numpy(c2).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for j in range(3):
+        top = np.abs(vals[:, :, j * 128:(j + 1) * 128]).max(axis=(2, 3))
+        assert np.all((top > 224) & (top <= 448))
+    exact = x.astype(np.float64) / np.repeat(d2, 128, axis=2)[:, :, :260, None]
+    np.testing.assert_array_equal(scaled, exact)

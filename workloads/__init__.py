@@ -176,17 +176,23 @@ class BlockScaledInputs:
 
 
 def blockscaled_inputs(B: int, H: int, N: int, d: int, seed: int = 0,
-                       spread_log2: float = 1.5) -> BlockScaledInputs:
+                       spread_log2: float = 0.5, v_spread_log2: float = 1.0,
+                       v_pow2: bool = True) -> BlockScaledInputs:
     """Random operands for the block-scaled fp8 path: the per-tensor e4m3 codes of
     ``random_inputs`` and, for every 128-row block, a descale equal to the per-tensor one times
-    2^u with u uniform in [-spread_log2, spread_log2] (seeded; Q, K, V in that order)."""
+    2^u, u uniform in [-spread, spread] (seeded; Q, K, V in that order; ``v_spread_log2`` for
+    V).  With ``v_pow2`` the value descales are rounded to the nearest power of two."""
     base = random_inputs(B, H, N, d, "e4m3", seed)
     g = torch.Generator(device="cpu").manual_seed(seed + 9191)
     nblk = -(-N // 128)
     ds = []
-    for d0 in (base.descale_q, base.descale_k, base.descale_v):
-        u = (torch.rand((B, H, nblk), generator=g, dtype=torch.float64) * 2 - 1) * spread_log2
-        ds.append((d0 * torch.exp2(u)).to(torch.float32))
+    for i, d0 in enumerate((base.descale_q, base.descale_k, base.descale_v)):
+        spread = v_spread_log2 if i == 2 else spread_log2
+        u = (torch.rand((B, H, nblk), generator=g, dtype=torch.float64) * 2 - 1) * spread
+        e = math.log2(d0) + u
+        if i == 2 and v_pow2:
+            e = torch.round(e)
+        ds.append(torch.exp2(e).to(torch.float32))
     return BlockScaledInputs(base.q, base.k, base.v, *ds)
 
 
