@@ -257,9 +257,11 @@ def run_ours(args, w, world, rank, local):
         workspace = torch.empty(ea.split_workspace_bytes(w.B, w.H, w.N, w.d, splits),
                                 dtype=torch.uint8, device=dev)
 
+    pv16 = args.fp8_pv == "f16"
+
     def step():
         ea.fwd(q, k, v, causal=w.causal, scale=w.scale, descale=descale, out=o, lse=lse,
-               num_splits=splits, workspace=workspace)
+               num_splits=splits, workspace=workspace, pv16=pv16)
 
     for _ in range(args.warmup):
         step()
@@ -317,7 +319,7 @@ def run_ours(args, w, world, rank, local):
         s_cmp.wait_event(ev["out"][b])         # the D2H that last read outputs b is done
         with torch.cuda.stream(s_cmp):
             ea.fwd(dq[b], dk[b], dv[b], causal=w.causal, scale=w.scale, descale=descale,
-                   out=do[b], lse=dl[b], num_splits=splits, workspace=workspace)
+                   out=do[b], lse=dl[b], num_splits=splits, workspace=workspace, pv16=pv16)
         ev["cmp"][b].record(s_cmp)
         s_out.wait_event(ev["cmp"][b])
         with torch.cuda.stream(s_out):
@@ -371,6 +373,7 @@ def run_ours(args, w, world, rank, local):
                    "heads": w.H, "seq_len": w.N, "head_dim": w.d, "causal": w.causal,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "key_splits": args.splits,
+                   **({"pv_product": args.fp8_pv} if is_fp8 else {}),
                    "l2": "inputs larger than L2 (no flush)" if 3 * q.numel() * q.element_size()
                    > 129e6 else "inputs smaller than L2"},
         "pct_of_peak": 100.0 * achieved / peak,
@@ -402,6 +405,8 @@ def main():
     ap.add_argument("--cpu-s", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--ref-step-s", type=float, default=4.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fp8-pv", default="e4m3", choices=["e4m3", "f16"],
+                    help="fp8 operands: precision of the P V product")
     ap.add_argument("--traffic-bytes", type=float, default=None,
                     help="DRAM bytes per launch from an ncu capture of the current kernel")
     args = ap.parse_args()

@@ -27,6 +27,7 @@ FA_ERR_DEVICE_TIMEOUT = 5
 FA_QUANT_POW2_DESCALE = 1
 FA_DTYPE_BF16 = 0
 FA_DTYPE_FP8_E4M3 = 1
+FA_DTYPE_FP8_E4M3_PV16 = 2
 
 LIB_PATH = _build.LIB_PATH
 
@@ -51,7 +52,7 @@ SIGNATURES = {
                                         _c.c_void_p]),
     "fa_fwd_fp8_blockscaled": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
                                           _c.c_void_p, _c.c_int, _c.c_int, _c.c_int, _c.c_int,
-                                          _c.c_float, _c.c_int, _c.c_void_p, _c.c_void_p,
+                                          _c.c_float, _c.c_int, _c.c_int, _c.c_void_p, _c.c_void_p,
                                           _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_size_t,
                                           _c.c_void_p, _c.c_void_p]),
     "fa_quantize_e4m3": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_int,
@@ -148,11 +149,12 @@ def fa_fwd_split_noalloc(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, scale,
 
 def fa_fwd_fp8_blockscaled(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, scale, causal,
                            dq_blk_ptr, dk_blk_ptr, dv_blk_ptr, num_splits=1, workspace_ptr=None,
-                           workspace_bytes=0, status_ptr=None, stream=None) -> int:
+                           workspace_bytes=0, status_ptr=None, stream=None,
+                           dtype=FA_DTYPE_FP8_E4M3) -> int:
     return lib().fa_fwd_fp8_blockscaled(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, scale,
-                                        int(causal), dq_blk_ptr, dk_blk_ptr, dv_blk_ptr,
-                                        int(num_splits), workspace_ptr, int(workspace_bytes),
-                                        status_ptr, stream)
+                                        int(causal), int(dtype), dq_blk_ptr, dk_blk_ptr,
+                                        dv_blk_ptr, int(num_splits), workspace_ptr,
+                                        int(workspace_bytes), status_ptr, stream)
 
 
 def fa_quantize_e4m3(x_ptr, codes_ptr, descales_ptr, B, H, N, d, signs_ptr=None, flags=0,
@@ -176,10 +178,11 @@ def version() -> int:
 
 
 def fwd(q, k, v, causal: bool = False, scale: float | None = None, descale=None, out=None,
-        lse=None, status=None, num_splits: int = 1, workspace=None):
+        lse=None, status=None, num_splits: int = 1, workspace=None, pv16: bool = False):
     """Attention forward on torch CUDA tensors [B, H, N, d]; returns (o bf16, lse fp32).
 
-    ``descale`` = (dq, dk, dv) for float8_e4m3fn operands.  ``out``/``lse`` may be given
+    ``descale`` = (dq, dk, dv) for float8_e4m3fn operands; both of their products are fp8
+    unless ``pv16`` asks for an f16 P V product (P rounded to f16: slower, more accurate).  ``out``/``lse`` may be given
     (contiguous, right shape and dtype) to avoid allocation.  ``status`` is an optional int32
     CUDA tensor of one element the kernel sets to FA_ERR_DEVICE_TIMEOUT if a wait runs out.
     ``num_splits`` > 1 splits each query tile's keys over that many CTAs and merges the partial
@@ -199,7 +202,7 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, descale=None,
     if q.dtype == torch.bfloat16:
         dtype = FA_DTYPE_BF16
     elif q.dtype == torch.float8_e4m3fn:
-        dtype = FA_DTYPE_FP8_E4M3
+        dtype = FA_DTYPE_FP8_E4M3_PV16 if pv16 else FA_DTYPE_FP8_E4M3
     else:
         raise ValueError(f"unsupported operand dtype {q.dtype}")
     B, H, N, d = q.shape
@@ -271,7 +274,7 @@ def quantize_e4m3(x, signs=None, pow2: bool = False, codes=None, descales=None):
 
 def fwd_fp8_blockscaled(q, k, v, dq_blk, dk_blk, dv_blk, causal: bool = False,
                         scale: float | None = None, out=None, lse=None, status=None,
-                        num_splits: int = 1, workspace=None):
+                        num_splits: int = 1, workspace=None, pv16: bool = False):
     """Attention forward on float8_e4m3fn CUDA tensors with per-block descales
     (fp32 [B, H, ceil(N / 128)] each, as ``quantize_e4m3`` returns); returns (o bf16, lse)."""
     import torch
@@ -311,7 +314,8 @@ def fwd_fp8_blockscaled(q, k, v, dq_blk, dk_blk, dv_blk, causal: bool = False,
         rc = fa_fwd_fp8_blockscaled(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                     lse.data_ptr(), B, H, N, d, float(scale), causal,
                                     dq_blk.data_ptr(), dk_blk.data_ptr(), dv_blk.data_ptr(),
-                                    num_splits, ws_ptr, ws_bytes, st, stream)
+                                    num_splits, ws_ptr, ws_bytes, st, stream,
+                                    FA_DTYPE_FP8_E4M3_PV16 if pv16 else FA_DTYPE_FP8_E4M3)
     _check(rc, "fa_fwd_fp8_blockscaled")
     return out, lse
 

@@ -89,7 +89,7 @@ struct BlockScales {
   const float* dv;
 };
 
-template <int D, bool FP8, bool CAUSAL>
+template <int D, bool FP8, bool CAUSAL, bool PV16>
 int launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
            float c, float out_mult, int* status, int splits, float* o_part, float* lse_part,
            const BlockScales* bs, cudaStream_t stream) {
@@ -99,8 +99,9 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   if (!encode_operand_map(&mq, q, elem, D, N, bh) || !encode_operand_map(&mk, k, elem, D, N, bh) ||
       !encode_operand_map(&mv, v, elem, D, N, bh))
     return FA_ERR_CUDA;
-  auto kern = fa_fwd_kernel<D, FP8, CAUSAL>;
-  constexpr int smem = smem_bytes<D, FP8>();
+  auto kern = fa_fwd_kernel<D, FP8, CAUSAL, PV16>;
+  constexpr int smem = smem_bytes<D, FP8, PV16>();
+  static_assert(smem <= 227 * 1024, "shared memory per CTA");
   // one CTA per SM (the kernel takes all 512 TMEM columns): ask for > half the SM's smem
   constexpr int smem_request = smem > 120 * 1024 ? smem : 120 * 1024;
   int dev = 0;
@@ -135,13 +136,14 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool PV16 = false>
 int launch_mask(int causal, const void* q, const void* k, const void* v, void* o, float* lse,
                 int B, int H, int N, float c, float om, int* st, int splits, float* op,
                 float* lp, const BlockScales* bs, cudaStream_t s) {
-  return causal
-             ? launch<D, FP8, true>(q, k, v, o, lse, B, H, N, c, om, st, splits, op, lp, bs, s)
-             : launch<D, FP8, false>(q, k, v, o, lse, B, H, N, c, om, st, splits, op, lp, bs, s);
+  return causal ? launch<D, FP8, true, PV16>(q, k, v, o, lse, B, H, N, c, om, st, splits, op, lp,
+                                             bs, s)
+                : launch<D, FP8, false, PV16>(q, k, v, o, lse, B, H, N, c, om, st, splits, op,
+                                              lp, bs, s);
 }
 
 // Merge of key splits ("FlashAttention · InkStack", section 2.2: key blocks can be processed
@@ -216,14 +218,16 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
              const BlockScales* bs = nullptr) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
-  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP8_E4M3) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP8_E4M3 && dtype != FA_DTYPE_FP8_E4M3_PV16)
+    return FA_ERR_INVALID_ARG;
+  const bool fp8 = dtype != FA_DTYPE_BF16;
   if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
   if (splits < 1 || splits > kMaxSplits) return FA_ERR_INVALID_ARG;
   float dq = 1.f, dk = 1.f, dv = 1.f;
   int* status = nullptr;
   if (opts) {
     status = opts->dev_status;
-    if (dtype == FA_DTYPE_FP8_E4M3) {
+    if (fp8) {
       dq = opts->descale_q;
       dk = opts->descale_k;
       dv = opts->descale_v;
@@ -246,7 +250,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     lse_part = o_part + static_cast<size_t>(splits) * B * H * N * d;
   }
   if (bs) {
-    if (dtype != FA_DTYPE_FP8_E4M3 || !bs->dq || !bs->dk || !bs->dv) return FA_ERR_INVALID_ARG;
+    if (!fp8 || !bs->dq || !bs->dk || !bs->dv) return FA_ERR_INVALID_ARG;
     if (!aligned(bs->dq, 4) || !aligned(bs->dk, 4) || !aligned(bs->dv, 4))
       return FA_ERR_MISALIGNED;
   }
@@ -263,11 +267,16 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
                                           splits, o_part, lse_part, nullptr, s)
                  : launch_mask<128, false>(causal, q, k, v, o, lse, B, H, N, cf, 1.f, status,
                                            splits, o_part, lse_part, nullptr, s);
+  } else if (dtype == FA_DTYPE_FP8_E4M3_PV16) {
+    rc = d == 64 ? launch_mask<64, true, true>(causal, q, k, v, o, lse, B, H, N, cf, dv, status,
+                                               splits, o_part, lse_part, bs, s)
+                 : launch_mask<128, true, true>(causal, q, k, v, o, lse, B, H, N, cf, dv, status,
+                                                splits, o_part, lse_part, bs, s);
   } else {
-    rc = d == 64 ? launch_mask<64, true>(causal, q, k, v, o, lse, B, H, N, cf, dv, status,
-                                         splits, o_part, lse_part, bs, s)
-                 : launch_mask<128, true>(causal, q, k, v, o, lse, B, H, N, cf, dv, status,
-                                          splits, o_part, lse_part, bs, s);
+    rc = d == 64 ? launch_mask<64, true, false>(causal, q, k, v, o, lse, B, H, N, cf, dv, status,
+                                                splits, o_part, lse_part, bs, s)
+                 : launch_mask<128, true, false>(causal, q, k, v, o, lse, B, H, N, cf, dv,
+                                                 status, splits, o_part, lse_part, bs, s);
   }
   if (rc != FA_OK || splits == 1) return rc;
   const long long rows = static_cast<long long>(B) * H * N;
@@ -305,16 +314,17 @@ int fa_fwd_split(const void* q, const void* k, const void* v, void* o, float* ls
 }
 
 int fa_fwd_fp8_blockscaled(const void* q, const void* k, const void* v, void* o, float* lse,
-                           int B, int H, int N, int d, float scale, int causal,
+                           int B, int H, int N, int d, float scale, int causal, int dtype,
                            const float* descale_q_blk, const float* descale_k_blk,
                            const float* descale_v_blk, int num_splits, void* workspace,
                            size_t workspace_bytes, int* dev_status, void* stream) {
+  if (dtype != FA_DTYPE_FP8_E4M3 && dtype != FA_DTYPE_FP8_E4M3_PV16) return FA_ERR_INVALID_ARG;
   fa_fwd_opts opts;
   opts.descale_q = opts.descale_k = opts.descale_v = 1.f;
   opts.dev_status = dev_status;
   const BlockScales bs{descale_q_blk, descale_k_blk, descale_v_blk};
-  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, FA_DTYPE_FP8_E4M3, &opts,
-                  num_splits, workspace, workspace_bytes, stream, &bs);
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, &opts, num_splits,
+                  workspace, workspace_bytes, stream, &bs);
 }
 
 int fa_quantize_e4m3(const void* x, void* codes, float* descales, int B, int H, int N, int d,

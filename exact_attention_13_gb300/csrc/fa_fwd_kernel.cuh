@@ -10,14 +10,16 @@
 //
 //   warps 0-3  softmax, Q tile 0     one thread per query row: reads its S row from TMEM,
 //   warps 4-7  softmax, Q tile 1     updates (m, l), rescales its O row when m grew, writes the
-//                                    bf16/e4m3 probabilities back into the S columns, and at the
+//                                    bf16/f16/e4m3 probabilities back into the S columns, and at the
 //                                    end normalises O, stores it and the row's log-sum-exp
 //   warp  8    TMA producer          Q tiles once, then K_j, V_j into the ring (full/empty
 //                                    mbarriers, "FlashAttention · InkStack", section 3.2.1)
 //   warp  9    MMA issuer            one thread issues S_h = Q_h K_j^T (both operands in smem)
 //                                    and O_h += P_h V_j (P from TMEM, V from smem), and owns the
 //                                    TMEM allocation
-//   warps 10-11 idle
+//   warps 10-11 V converters         (fp8 operands with an f16 P V product only) widen each
+//                                    e4m3 V block to f16 in shared memory for the PV MMAs;
+//                                    otherwise idle
 //
 // TMEM (512 columns x 128 lanes, fp32 cells): S_0 at columns 0-127, S_1 at 128-255 (P_h is
 // written over S_h), O_0 at 256.., O_1 at 384.. .  Lane i holds row i of each tile.
@@ -101,6 +103,9 @@ constexpr float kRescaleLog2 = EXATTN_RESCALE_LOG2;
 #ifndef EXATTN_KV_SLOTS_D128
 #define EXATTN_KV_SLOTS_D128 4
 #endif
+#ifndef EXATTN_KV_SLOTS_PV16
+#define EXATTN_KV_SLOTS_PV16 6
+#endif
 template <bool FP8>
 __host__ __device__ constexpr int l2_prefetch_blocks() {
 #ifdef EXATTN_L2_PREFETCH_BLOCKS
@@ -150,8 +155,10 @@ __host__ __device__ constexpr float p_offset_log2() {
   return FP8 ? 8.f : 0.f;
 }
 
-// Compile-time geometry of one instance.
-template <int D, bool FP8>
+// Compile-time geometry of one instance.  PV16 (fp8 operands only): the P V product runs in
+// f16 -- P rounded to f16 instead of e4m3, V widened from e4m3 to f16 in shared memory by a
+// converter warp -- while S = Q K^T stays an fp8 product.
+template <int D, bool FP8, bool PV16 = false>
 struct Geo {
   static constexpr int kElem = FP8 ? 1 : 2;                 // bytes per operand element
   static constexpr int kRowBytes = D * kElem;               // bytes of one operand row
@@ -159,15 +166,24 @@ struct Geo {
   static constexpr int kBoxes = kRowBytes / kSwBytes;       // TMA boxes per 128-row tile
   static constexpr int kBoxElems = kSwBytes / kElem;        // inner box extent (elements)
   static constexpr int kTileBytes = kTileRows * kRowBytes;  // one 128-row operand tile
-  static constexpr int kSlots = (FP8 || D == 64) ? 8 : EXATTN_KV_SLOTS_D128;  // K/V ring depth
+  static constexpr bool kPv16 = FP8 && PV16;
+  static constexpr bool kPE4m3 = FP8 && !PV16;              // P stored as e4m3
+  static constexpr int kSlots = (FP8 && D == 128 && PV16)
+                                    ? EXATTN_KV_SLOTS_PV16
+                                    : ((FP8 || D == 64) ? 8 : EXATTN_KV_SLOTS_D128);  // ring depth
   static constexpr int kQBytes = 2 * kTileBytes;
   static constexpr int kRingBytes = kSlots * kTileBytes;
+  // f16 copies of V (PV16): two buffers, each 128 keys x D in 128-byte swizzled boxes of 64
+  // columns, the layout of a bf16 V tile
+  static constexpr int kV16TileBytes = kTileRows * D * 2;
+  static constexpr int kV16Bytes = kPv16 ? 2 * kV16TileBytes : 0;
   static constexpr uint32_t kSwMode = kSwBytes == 128 ? kSwizzle128B : kSwizzle64B;
   static constexpr int kKStepBytes = 32;                    // K extent of one MMA, in bytes
   static constexpr int kKStepsS = kRowBytes / kKStepBytes;  // MMAs per S = Q K^T
-  static constexpr int kKeysPerPv = FP8 ? 32 : 16;          // keys per PV MMA
+  static constexpr int kKeysPerPv = kPE4m3 ? 32 : 16;       // keys per PV MMA
   static constexpr int kPvSteps = kTileRows / kKeysPerPv;   // MMAs per O += P V
-  static constexpr int kPCols = FP8 ? 32 : 64;              // TMEM columns of one P row
+  static constexpr int kPCols = kPE4m3 ? 32 : 64;           // TMEM columns of one P row
+  static constexpr int kPvSwBytes = kPv16 ? 128 : kSwBytes; // swizzle span of the PV B tile
   static constexpr uint32_t kIdescS = instr_desc(128, 128, FP8 ? 0 : 1, false, false);
   static constexpr uint32_t kIdescPV = instr_desc(128, D, FP8 ? 0 : 1, false, true);
 };
@@ -181,15 +197,17 @@ struct Ctrl {
   uint64_t s_full[2];
   uint64_t p_full[2][2];  // [tile][half of the keys]
   uint64_t o_full[2];
+  uint64_t v16_full[2];   // f16 V buffer b written (PV16)
+  uint64_t v16_empty[2];  // f16 V buffer b no longer read by the MMAs (PV16)
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool PV16 = false>
 constexpr int smem_bytes() {
-  using G = Geo<D, FP8>;
-  return G::kQBytes + G::kRingBytes + (int)sizeof(Ctrl<G::kSlots>) + 1024;
+  using G = Geo<D, FP8, PV16>;
+  return G::kQBytes + G::kRingBytes + G::kV16Bytes + (int)sizeof(Ctrl<G::kSlots>) + 1024;
 }
 
 // Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting or the wait ran out.
@@ -226,7 +244,9 @@ __device__ __forceinline__ int kv_blocks_for_tile(int row0, int n) {
 // to bf16 (or e4m3) and written over the S columns in TMEM in two halves of 64 keys; after the
 // last half (or after each half when P_PARTS == 2) the warp publishes on the P barrier.  Returns
 // the fp32 sum of the unrounded p.
-template <bool MASKED, bool FP8, int P_PARTS, int EMU_EVERY>
+enum class PFmt { kBf16, kF16, kE4m3 };
+
+template <bool MASKED, PFmt PF, int P_PARTS, int EMU_EVERY>
 __device__ __forceinline__ float exp_and_publish(float (&s)[128], float c, float m, int lim,
                                                  uint32_t t_s, uint32_t bar0, uint32_t bar1,
                                                  int lane) {
@@ -246,7 +266,7 @@ __device__ __forceinline__ float exp_and_publish(float (&s)[128], float c, float
       s[i] = p;
       ps[i % 8] += p;
     }
-    if constexpr (FP8) {
+    if constexpr (PF == PFmt::kE4m3) {
       uint32_t r[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -257,7 +277,9 @@ __device__ __forceinline__ float exp_and_publish(float (&s)[128], float c, float
     } else {
       uint32_t r[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) r[i] = pack_bf16x2(s[64 * half + 2 * i], s[64 * half + 2 * i + 1]);
+      for (int i = 0; i < 32; ++i)
+        r[i] = PF == PFmt::kF16 ? pack_f16x2(s[64 * half + 2 * i], s[64 * half + 2 * i + 1])
+                                : pack_bf16x2(s[64 * half + 2 * i], s[64 * half + 2 * i + 1]);
       tmem_st32(t_s + 32 * half, r);
     }
     if (P_PARTS == 2 || half == 1) {
@@ -274,11 +296,12 @@ __device__ __forceinline__ float exp_and_publish(float (&s)[128], float c, float
   return ps[0];
 }
 
-template <int D, bool FP8, bool CAUSAL>
+template <int D, bool FP8, bool CAUSAL, bool PV16 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const KernelArgs args) {
-  using G = Geo<D, FP8>;
+  using G = Geo<D, FP8, PV16>;
+  constexpr PFmt kPFmt = !FP8 ? PFmt::kBf16 : (PV16 ? PFmt::kF16 : PFmt::kE4m3);
   constexpr int kPHalves = p_parts<FP8>();
   constexpr int kL2PrefetchBlocks = l2_prefetch_blocks<FP8>();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -286,7 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* s_q = smem;                          // two Q tiles
   uint8_t* s_ring = smem + G::kQBytes;          // K/V slots
-  Ctrl<G::kSlots>* ctl = reinterpret_cast<Ctrl<G::kSlots>*>(s_ring + G::kRingBytes);
+  uint8_t* s_v16 = s_ring + G::kRingBytes;      // f16 V buffers (PV16)
+  Ctrl<G::kSlots>* ctl = reinterpret_cast<Ctrl<G::kSlots>*>(s_v16 + G::kV16Bytes);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -327,6 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&ctl->p_full[h][0]), 4);  // one arrival per softmax warp
       mbar_init(smem_u32(&ctl->p_full[h][1]), 4);
       mbar_init(smem_u32(&ctl->o_full[h]), 1);
+      mbar_init(smem_u32(&ctl->v16_full[h]), 2);  // one arrival per converter warp
+      mbar_init(smem_u32(&ctl->v16_empty[h]), 1);
     }
     mbar_init(smem_u32(&ctl->drain), 1);
     ctl->abort = 0;
@@ -448,9 +474,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       // halves of 64 keys; the MMAs of the first half start while the second is computed.
       auto issue_pv = [&](int h, int j) -> bool {
         const int t = 2 * j + 1;
-        if (!wait_kv(t)) return false;
+        uint32_t v_tile;
+        if constexpr (G::kPv16) {
+          if (!wait_phase(smem_u32(&ctl->v16_full[j & 1]), (j >> 1) & 1, abort_flag,
+                          args.status))
+            return false;
+          tc_fence_after();
+          v_tile = smem_u32(s_v16) + (j & 1) * G::kV16TileBytes;
+          // both converter warps are done with the e4m3 copy: hand its slot back
+          const bool first_user = (h == 0) || (j >= nkv[0]);
+          if (first_user) mbar_arrive(smem_u32(&ctl->kv_empty[t % G::kSlots]));
+        } else {
+          if (!wait_kv(t)) return false;
+          v_tile = ring_base + (t % G::kSlots) * G::kTileBytes;
+        }
         EXATTN_TRACE_EVENT(8, h, j);
-        const uint32_t v_tile = ring_base + (t % G::kSlots) * G::kTileBytes;
 #pragma unroll
         for (int half = 0; half < kPHalves; ++half) {
           if (!wait_phase(smem_u32(&ctl->p_full[h][half]), j & 1, abort_flag, args.status))
@@ -460,11 +498,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < G::kPvSteps / kPHalves; ++kk) {
             const int kb = half * (G::kPvSteps / kPHalves) + kk;
-            const uint64_t dv = smem_desc(v_tile + kb * G::kKeysPerPv * G::kSwBytes,
-                                          kTileRows * G::kSwBytes, 8 * G::kSwBytes, G::kSwMode);
+            const uint64_t dv =
+                smem_desc(v_tile + kb * G::kKeysPerPv * G::kPvSwBytes, kTileRows * G::kPvSwBytes,
+                          8 * G::kPvSwBytes, G::kPv16 ? kSwizzle128B : G::kSwMode);
             const uint32_t a = tmem + h * 128 + kb * 8;
             const uint32_t acc = (j > 0 || kb > 0) ? 1u : 0u;
-            if constexpr (FP8)
+            if constexpr (G::kPE4m3)
               mma_f8_ts(tmem + 256 + h * 128, a, dv, G::kIdescPV, acc);
             else
               mma_f16_ts(tmem + 256 + h * 128, a, dv, G::kIdescPV, acc);
@@ -473,7 +512,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         EXATTN_TRACE_EVENT(5, h, j);
         if (j == nkv[h] - 1) tc_commit(smem_u32(&ctl->o_full[h]));
         const bool last_user = (h == 1) || (j >= nkv[1]);
-        if (last_user) tc_commit(smem_u32(&ctl->kv_empty[t % G::kSlots]));
+        // PV16: the converter has already released the e4m3 slot; free the f16 copy instead
+        if (last_user)
+          tc_commit(smem_u32(G::kPv16 ? &ctl->v16_empty[j & 1] : &ctl->kv_empty[t % G::kSlots]));
         return true;
       };
 
@@ -492,6 +533,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_commit(smem_u32(&ctl->drain));
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(smem_u32(&ctl->drain), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+  } else {
+    if constexpr (G::kPv16) {
+      // ========================================================== V converters (PV16)
+      // Warps 10 and 11 widen each e4m3 V block to f16 (rows [0, 64) and [64, 128)) in one of
+      // two buffers; the MMA thread frees the e4m3 ring slot once both halves are written.
+      // Source: 128 rows of D bytes, swizzled over spans of kSwBytes (128 B for D = 128, 64 B
+      // for D = 64).  Destination: boxes of 64 columns (128-byte rows, 128-byte swizzle).  Each
+      // lane moves 16-element chunks: one 16-byte load, eight exact widenings, two 16-byte
+      // stores.
+      constexpr int kChunks = D / 16;            // 16-element chunks per row
+      constexpr int kRowsPerPass = 32 / kChunks;
+      const int row_begin = (warp - 10) * (kTileRows / 2);
+      const int c = lane % kChunks;
+      const int box_off = (c / 4) * (kTileRows * 128);
+      const int cc = 2 * (c % 4);
+      bool ok = true;
+      for (int j = 0; j < nkv_load && ok; ++j) {
+        const int t = 2 * j + 1;
+        const int slot = t % G::kSlots;
+        ok = wait_phase(smem_u32(&ctl->kv_full[slot]), (t / G::kSlots) & 1, abort_flag,
+                        args.status);
+        if (ok && j >= 2)
+          ok = wait_phase(smem_u32(&ctl->v16_empty[j & 1]), ((j >> 1) - 1) & 1, abort_flag,
+                          args.status);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        fence_proxy_async_smem();
+        const uint8_t* src = s_ring + slot * G::kTileBytes;
+        uint8_t* dst = s_v16 + (j & 1) * G::kV16TileBytes + box_off;
+#pragma unroll 2
+        for (int r = row_begin + lane / kChunks; r < row_begin + kTileRows / 2;
+             r += kRowsPerPass) {
+          const int c_phys = D == 128 ? (c ^ (r & 7)) : (c ^ ((r >> 1) & 3));
+          const uint4 raw = *reinterpret_cast<const uint4*>(src + r * G::kRowBytes + c_phys * 16);
+          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+          uint32_t hx[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            hx[2 * i] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] & 0xFFFFu));
+            hx[2 * i + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] >> 16));
+          }
+          // elements 16c .. 16c+15 = box c / 4, 16-byte chunks cc and cc + 1 of the row
+          uint8_t* row = dst + r * 128;
+          *reinterpret_cast<uint4*>(row + ((cc ^ (r & 7)) * 16)) =
+              make_uint4(hx[0], hx[1], hx[2], hx[3]);
+          *reinterpret_cast<uint4*>(row + (((cc + 1) ^ (r & 7)) * 16)) =
+              make_uint4(hx[4], hx[5], hx[6], hx[7]);
+        }
+        // the MMAs read the f16 copy through the async proxy
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->v16_full[j & 1]));
       }
     }
   }
@@ -616,10 +711,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t pb1 = smem_u32(&ctl->p_full[h][kPHalves == 2 ? 1 : 0]);
       const float m_shift = m_run - bias_j;
       const float rowsum =
-          masked ? exp_and_publish<true, FP8, kPHalves, 0>(s, c_j, m_shift, lim, t_s, pb0, pb1,
-                                                           lane)
-                 : exp_and_publish<false, FP8, kPHalves, EXATTN_EMU_EVERY>(s, c_j, m_shift, lim,
-                                                                           t_s, pb0, pb1, lane);
+          masked ? exp_and_publish<true, kPFmt, kPHalves, 0>(s, c_j, m_shift, lim, t_s, pb0, pb1,
+                                                             lane)
+                 : exp_and_publish<false, kPFmt, kPHalves, EXATTN_EMU_EVERY>(s, c_j, m_shift, lim,
+                                                                             t_s, pb0, pb1, lane);
       if (threadIdx.x % 128 == 0) EXATTN_TRACE_EVENT(3, h, j);
       l_run = fmaf(rowsum, l_mult, l_run);
     }

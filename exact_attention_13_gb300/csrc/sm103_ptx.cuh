@@ -318,6 +318,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Pack two fp32 into f16x2 (round to nearest even): `lo` in bits 0-15, `hi` in bits 16-31.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Widen two e4m3 values (byte 0 -> bits 0-15, byte 1 -> bits 16-31) to f16x2; exact, since
+// every e4m3 value is an f16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
+}
+
 // Pack four fp32 into e4m3x4 (round to nearest even, saturating): a in byte 0 .. d in byte 3.
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
   uint32_t r;

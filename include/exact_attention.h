@@ -46,8 +46,14 @@ extern "C" {
 #endif
 
 typedef enum {
-  FA_DTYPE_BF16 = 0,     /* q, k, v are bf16 */
-  FA_DTYPE_FP8_E4M3 = 1  /* q, k, v are fp8 e4m3fn with per-tensor fp32 descales */
+  FA_DTYPE_BF16 = 0,          /* q, k, v are bf16 */
+  FA_DTYPE_FP8_E4M3 = 1,      /* q, k, v are fp8 e4m3fn with fp32 descales; both products are
+                                 fp8 ("FlashAttention · InkStack", section 3.3): P is rounded to
+                                 e4m3, up to 2^-4 relative per probability, so a row whose mass
+                                 sits on a few keys carries that error on O */
+  FA_DTYPE_FP8_E4M3_PV16 = 2  /* as FP8_E4M3, but the P V product is f16: P rounded to f16, V
+                                 widened exactly from e4m3 in shared memory (slower; S = Q K^T
+                                 stays an fp8 product) */
 } fa_dtype;
 
 typedef enum {
@@ -150,6 +156,7 @@ FA_API int fa_fwd_split_noalloc(const void* q, const void* k, const void* v, voi
  * row i of head (b, h) is code * descale_X_blk[(b * H + h) * nblk + i / 128], nblk = ceil(N / 128).
  * Score block (i, j) is then scale * dq_i * dk_j * (q . k) and the output sum_j P_ij dv_j V_j.
  *   q, k, v           : device pointers, [B, H, N, d] e4m3fn codes (16-byte aligned)
+ *   dtype             : FA_DTYPE_FP8_E4M3 or FA_DTYPE_FP8_E4M3_PV16 (precision of P V)
  *   descale_*_blk     : device pointers, [B, H, nblk] fp32 (4-byte aligned); every descale must
  *                       be finite and > 0 (fa_quantize_e4m3 writes such arrays), otherwise the
  *                       output is undefined (the kernel still runs to completion).  The value
@@ -161,7 +168,7 @@ FA_API int fa_fwd_split_noalloc(const void* q, const void* k, const void* v, voi
  */
 FA_API int fa_fwd_fp8_blockscaled(const void* q, const void* k, const void* v, void* o,
                                   float* lse, int B, int H, int N, int d, float scale,
-                                  int causal, const float* descale_q_blk,
+                                  int causal, int dtype, const float* descale_q_blk,
                                   const float* descale_k_blk, const float* descale_v_blk,
                                   int num_splits, void* workspace, size_t workspace_bytes,
                                   int* dev_status, void* stream);

@@ -11,7 +11,7 @@ import torch
 
 from oracle import oracle
 from oracle import quantize as qz
-from tests.parity import compare
+from tests.parity import compare, compare_e4m3_p
 from workloads import blockscaled_inputs, hadamard_signs, outlier_inputs, quantize_e4m3, \
     random_inputs, sample_rows
 
@@ -113,16 +113,25 @@ BLOCK_SHAPES = [
 @pytest.mark.parametrize("B,H,N,d,causal,splits,spread", BLOCK_SHAPES,
                          ids=[f"B{b}H{h}N{n}d{d}-{'causal' if c else 'full'}-s{s}-u{u:g}"
                               for b, h, n, d, c, s, u in BLOCK_SHAPES])
-def test_blockscaled_attention_parity(ea, B, H, N, d, causal, splits, spread):
+@pytest.mark.parametrize("pv16", [False, True], ids=["pv-fp8", "pv-f16"])
+def test_blockscaled_attention_parity(ea, B, H, N, d, causal, splits, spread, pv16):
+    """Strict fp8 tolerance for the f16 P V product and for non-causal rows; causal rows with
+    an fp8 P V product are held to the e4m3-rounding bound of P (compare_e4m3_p)."""
     inp = blockscaled_inputs(B, H, N, d, seed=11 * N + d + int(causal), spread_log2=spread)
     dev = [getattr(inp, n).to(DEV) for n in ("q", "k", "v", "dq", "dk", "dv")]
-    o, lse = ea.fwd_fp8_blockscaled(*dev, causal=causal, num_splits=splits)
+    o, lse = ea.fwd_fp8_blockscaled(*dev, causal=causal, num_splits=splits, pv16=pv16)
     torch.cuda.synchronize()
     scale = 1.0 / math.sqrt(d)
     o_ref, l_ref = oracle.get().attention_fwd_blockscaled(
         inp.raw("q"), inp.raw("k"), inp.raw("v"), scale, causal, "e4m3", inp.dq.double().numpy(),
         inp.dk.double().numpy(), inp.dv.double().numpy(), 128)
-    compare(o, lse, o_ref, l_ref, "e4m3", f"{(B, H, N, d, causal, splits)}")
+    where = f"{(B, H, N, d, causal, splits, pv16)}"
+    if pv16 or not causal:
+        compare(o, lse, o_ref, l_ref, "e4m3", where)
+    else:
+        v = inp.v.to(torch.float64).numpy() * np.repeat(inp.dv.double().numpy(), 128,
+                                                        axis=2)[:, :, :N, None]
+        compare_e4m3_p(o, lse, o_ref, l_ref, float(np.abs(v).max()), where)
 
 
 def test_blockscaled_arbitrary_value_descales(ea):
@@ -191,6 +200,12 @@ def test_fp8_accuracy_study(ea):
     qh, dqh = ea.quantize_e4m3(q, signs=signs)
     kh, dkh = ea.quantize_e4m3(k, signs=signs)
     res["fp8_block_hadamard"] = rmse(ea.fwd_fp8_blockscaled(qh, kh, vb, dqh, dkh, dv)[0])
+    # the same three fp8 variants with an f16 P V product
+    res["fp8_per_tensor_pv16"] = rmse(ea.fwd(*(c.to(DEV) for c, _ in pt),
+                                             descale=tuple(s for _, s in pt), pv16=True)[0])
+    res["fp8_block_pv16"] = rmse(ea.fwd_fp8_blockscaled(qb, kb, vb, dq, dk, dv, pv16=True)[0])
+    res["fp8_block_hadamard_pv16"] = rmse(ea.fwd_fp8_blockscaled(qh, kh, vb, dqh, dkh, dv,
+                                                                 pv16=True)[0])
     torch.cuda.synchronize()
     print("RMSE", res)
     assert res["bf16"] < 1e-3
