@@ -161,8 +161,9 @@ def kernel_sources_sha256() -> str:
     return h.hexdigest()
 
 
-def measured_traffic(workload: str, override):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on these sources."""
+def measured_traffic(workload: str, override, variant: str = ""):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on these sources
+    (entries are keyed by workload, plus ":<variant>" for a non-default kernel variant)."""
     if override is not None:
         return override
     path = os.path.join(ROOT, "profiles", "fa_fwd_traffic.json")
@@ -170,7 +171,7 @@ def measured_traffic(workload: str, override):
         return None
     with open(path) as f:
         rec = json.load(f)
-    ent = rec.get(workload)
+    ent = rec.get(workload + (f":{variant}" if variant else ""))
     if not ent or ent.get("kernel_sources_sha256") != kernel_sources_sha256():
         return None
     return ent.get("dram_bytes_per_launch")
@@ -352,12 +353,19 @@ def run_ours(args, w, world, rank, local):
         return
     pk = peaks()
     is_fp8 = w.dtype == "e4m3"
-    peak = pk["bf16"] * (FP8_OVER_BF16 if is_fp8 else 1.0)
+    if is_fp8 and pv16:
+        # half the flops (Q K^T) at the fp8 rate, half (P V) at the f16 rate: the time-weighted
+        # peak is 1 / (0.5 / (2 P) + 0.5 / P) = 4 P / 3
+        peak = pk["bf16"] * 4.0 / 3.0
+        peak_note = " x 4/3 (Q K^T fp8 at 2x, P V f16 at 1x)"
+    else:
+        peak = pk["bf16"] * (FP8_OVER_BF16 if is_fp8 else 1.0)
+        peak_note = " x 2 (nominal fp8:bf16)" if is_fp8 else ""
     achieved = flops_rank / (ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": measured_traffic(w.name, args.traffic_bytes),
-                "peak_kind": (f"{pk['source']} cuBLAS bf16 burst"
-                              + (" x 2 (nominal fp8:bf16)" if is_fp8 else "")),
+                "frac": achieved / peak, "traffic": measured_traffic(w.name, args.traffic_bytes,
+                                                      "pv16" if is_fp8 and pv16 else ""),
+                "peak_kind": f"{pk['source']} cuBLAS bf16 burst" + peak_note,
                 "kernel": "exattn::fa_fwd_kernel"}
     # exp-unit bound at the clock seen during the run (informative)
     exps = w.B * w.H * (w.N * (w.N + 1) / 2 if w.causal else w.N * w.N)
@@ -393,6 +401,68 @@ def run_ours(args, w, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_quantize(args, w, world, rank, local):
+    """Time the fp8 block quantiser (fa_quantize_e4m3) on a bf16 operand of the workload's
+    shape: bytes moved per launch = 2 (bf16 in) + 1 (e4m3 out) per element, plus the descales."""
+    import torch
+
+    import exact_attention_13_gb300 as ea
+    from workloads import hadamard_signs, random_inputs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    x = random_inputs(w.B, w.H, w.N, w.d, "bf16", w.seed).q.to(dev)
+    codes = torch.empty(x.shape, dtype=torch.float8_e4m3fn, device=dev)
+    nblk = -(-w.N // 128)
+    ds = torch.empty((w.B, w.H, nblk), dtype=torch.float32, device=dev)
+    signs = hadamard_signs(w.d, w.seed).to(dev) if args.hadamard else None
+
+    def step():
+        ea.quantize_e4m3(x, signs=signs, codes=codes, descales=ds)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize()
+    ms = max_over_ranks(start.elapsed_time(end) / args.steps, world, dev)
+    if rank != 0:
+        return
+    nbytes = x.numel() * 3 + ds.numel() * 4 + (w.d * 4 if signs is not None else 0)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    pk = peaks()
+    line = {
+        "metric": "fp8 block quantisation GB/s (1 GPU, device-timed)", "value": gbs * world,
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16->e4m3", "data": "synthetic",
+        "config": {"workload": w.name, "shape": f"B{w.B} H{w.H} N{w.N} d{w.d}",
+                   "hadamard": bool(args.hadamard), "block_rows": 128,
+                   "l2": "input larger than L2 (no flush)" if x.numel() * 2 > 129e6
+                   else "input smaller than L2"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / pk["hbm_gbs"], "traffic": None,
+                     "peak_kind": f"{pk['source']} copy bandwidth",
+                     "kernel": "exattn::quantize_e4m3_kernel"},
+        "clocks": clk.summary(),
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -407,6 +477,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fp8-pv", default="e4m3", choices=["e4m3", "f16"],
                     help="fp8 operands: precision of the P V product")
+    ap.add_argument("--op", default="attention", choices=["attention", "quantize"],
+                    help="attention forward (default) or the fp8 block quantiser alone")
+    ap.add_argument("--hadamard", action="store_true",
+                    help="--op quantize: apply the incoherent (Hadamard) transform")
     ap.add_argument("--traffic-bytes", type=float, default=None,
                     help="DRAM bytes per launch from an ncu capture of the current kernel")
     args = ap.parse_args()
@@ -419,7 +493,10 @@ def main():
                       int(os.environ.get("RANK", "0")))
         return
     world, rank, local = init_dist()
-    run_ours(args, w, world, rank, local)
+    if args.op == "quantize":
+        run_quantize(args, w, world, rank, local)
+    else:
+        run_ours(args, w, world, rank, local)
     if world > 1:
         import torch.distributed as dist
 

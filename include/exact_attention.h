@@ -184,7 +184,8 @@ FA_API int fa_fwd_fp8_blockscaled(const void* q, const void* k, const void* v, v
  *                 Had is the Sylvester-Hadamard matrix), else X' = X
  *     descale   = max |X'_blk| / 448            (1 if the block is all zero); with
  *                 FA_QUANT_POW2_DESCALE, the smallest power of two >= that quotient
- *     code      = e4m3(X' / descale)            (round to nearest even, saturate at 448)
+ *     scale     = 448 / max |X'_blk|            (1 / descale with FA_QUANT_POW2_DESCALE)
+ *     code      = e4m3(X' * scale)              (round to nearest even, saturate at 448)
  * Apply the same `signs` to Q and K (QK^T is unchanged) and none to V.  Power-of-two value
  * descales let fa_fwd_fp8_blockscaled fold them into P exactly; other value descales add one
  * more e4m3 rounding of relative size up to 2^-4 to each probability.
@@ -194,8 +195,8 @@ FA_API int fa_fwd_fp8_blockscaled(const void* q, const void* k, const void* v, v
  *   signs    : device pointer to d fp32 values, each +1 or -1 (16-byte aligned), or NULL
  *   d        : 64 or 128; B * H <= 65535
  *   flags    : 0 or FA_QUANT_POW2_DESCALE (other bits: FA_ERR_INVALID_ARG)
- * Arithmetic is fp32 (correctly rounded quotients).  Returns an fa_status; asynchronous on
- * `stream` like fa_fwd.
+ * Arithmetic is fp32 (descale and scale correctly rounded once per block).  Returns an
+ * fa_status; asynchronous on `stream` like fa_fwd.
  */
 FA_API int fa_quantize_e4m3(const void* x, void* codes, float* descales, int B, int H, int N,
                             int d, const float* signs, int flags, void* stream);

@@ -14,15 +14,18 @@ What it computes (pages cited by title and section):
   kernel's business); the result is then rounded once to fp32, the precision the kernel keeps.
 * Block quantisation ("FlashAttention · InkStack", sections 3.3.1 "Block Quantization" and 3.3.3
   "Scaling"): every block of ``blk_rows`` consecutive rows of one head gets its own descale
-  ``amax(|X_blk|) / 448`` (448 is e4m3's largest finite value) and codes
-  ``e4m3(X / descale)``.  The arithmetic is fp32 (the descale is an fp32 quotient, the scaled
-  value an fp32 quotient), followed by round-to-nearest-even onto the e4m3 grid with results
-  beyond 448 clamped to 448.  A block whose amax is 0 gets descale 1.
+  ``amax(|X_blk|) / 448`` (448 is e4m3's largest finite value) and codes ``e4m3(X · scale)``
+  with ``scale = 448 / amax``.  The arithmetic is fp32: descale and scale are correctly rounded
+  fp32 quotients, X · scale an fp32 product, followed by round-to-nearest-even onto the e4m3
+  grid with results beyond 448 clamped to 448.  A block whose amax is 0 gets descale and scale 1.
 
 Readings where the pages leave a step open: the block is the attention kernel's 128-row tile;
-one sign vector s serves every head; the quotient is x / descale, not x times a reciprocal.
-Optionally (``pow2``) the descale is raised to the next power of two, a choice of this library
-for value blocks (e4m3's relative precision does not depend on the scale).
+one sign vector s serves every head; the pages only say that codes are the values scaled into
+e4m3's range by the amax / 448 factor, and this states that scaling as a multiplication by the
+fp32 reciprocal 448 / amax (one quotient per block instead of one per element).  Optionally
+(``pow2``) the descale is raised to the next power of two, a choice of this library for value
+blocks (e4m3's relative precision does not depend on the scale); the scale is then its exact
+reciprocal.
 """
 from __future__ import annotations
 
@@ -86,8 +89,8 @@ def block_quantize(x: np.ndarray, blk_rows: int = 128, signs=None, pow2: bool = 
     """Quantise X [B, H, N, d] block-wise; returns (codes uint8 [B,H,N,d], descales fp32
     [B,H,nblk], scaled fp64 [B,H,N,d]).  ``pow2`` rounds each descale up to a power of two.
 
-    ``scaled`` is the fp64 value of (transformed fp32 value) / (fp32 descale) before rounding,
-    for tests that have to tell rounding ties apart from errors.
+    ``scaled`` is the fp64 value of (transformed fp32 value) x (fp32 scale) before any
+    rounding, for tests that have to tell rounding ties apart from errors.
     """
     x = np.asarray(x)
     if signs is not None:
@@ -102,12 +105,16 @@ def block_quantize(x: np.ndarray, blk_rows: int = 128, signs=None, pow2: bool = 
     for j in range(nblk):
         blk = x32[:, :, j * blk_rows:(j + 1) * blk_rows]
         amax = np.abs(blk).max(axis=(2, 3))
-        ds = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+        one = np.float32(1.0)
+        ds = np.where(amax > 0, amax / np.float32(E4M3_MAX), one).astype(np.float32)
+        sc = np.where(amax > 0, np.float32(E4M3_MAX) / np.where(amax > 0, amax, one),
+                      one).astype(np.float32)
         if pow2:
             ds = np.exp2(np.ceil(np.log2(ds.astype(np.float64)))).astype(np.float32)
+            sc = (np.float32(1.0) / ds).astype(np.float32)
         descales[:, :, j] = ds
-        y = (blk / ds[:, :, None, None]).astype(np.float32)
+        y = (blk * sc[:, :, None, None]).astype(np.float32)
         codes[:, :, j * blk_rows:(j + 1) * blk_rows] = round_to_e4m3(y)[0]
-        scaled[:, :, j * blk_rows:(j + 1) * blk_rows] = blk.astype(np.float64) / ds[:, :, None,
-                                                                                   None]
+        scaled[:, :, j * blk_rows:(j + 1) * blk_rows] = (blk.astype(np.float64)
+                                                         * sc[:, :, None, None].astype(np.float64))
     return codes, descales, scaled

@@ -103,7 +103,8 @@ def _half_step(v):
 def test_block_quantize_scales_and_error_bound(signs):
     """Per 128-row block of each head: descale = amax / 448 in fp32 (the block maxima found
     here row by row), the block's largest element maps to +-448, and every code is within
-    half an e4m3 step of x / descale ("FlashAttention · InkStack", sections 3.3.1, 3.3.3)."""
+    half an e4m3 step (plus the fp32 rounding of the product) of x / descale
+    ("FlashAttention · InkStack", sections 3.3.1, 3.3.3)."""
     rng = np.random.default_rng(33)
     B, H, N, d = 2, 3, 300, 64
     x = rng.standard_normal((B, H, N, d)).astype(np.float32)
@@ -121,7 +122,10 @@ def test_block_quantize_scales_and_error_bound(signs):
                 want = np.float32(amax) / np.float32(448) if amax > 0 else np.float32(1)
                 assert descales[b, h, j] == want
     vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
-    assert np.all(np.abs(vals - scaled) <= _half_step(scaled) * (1 + 1e-12))
+    assert np.all(np.abs(vals - scaled) <= _half_step(scaled) * (1 + 1e-12)
+                  + np.abs(scaled) * 2.0 ** -23)
+    quot = xt.astype(np.float64) / np.repeat(descales, 128, axis=2)[:, :, :N, None]
+    np.testing.assert_allclose(scaled, quot, rtol=2.0 ** -22)
     assert np.abs(vals).max() == 448.0
     if not signs:
         assert vals[0, 1, 5, 7] == 448.0
@@ -150,3 +154,4 @@ def test_power_of_two_descales():
         assert np.all((top > 224) & (top <= 448))
     exact = x.astype(np.float64) / np.repeat(d2, 128, axis=2)[:, :, :260, None]
     np.testing.assert_array_equal(scaled, exact)
+    np.testing.assert_array_equal(c2, qz.round_to_e4m3(exact.astype(np.float32))[0])
