@@ -350,4 +350,175 @@ int oracle_attention_fwd_blockscaled(const void* q, const void* k, const void* v
     return run_job(&jb, nthreads);
 }
 
+/*
+ * Backward pass, in fp64 on the decoded operands ("FlashAttention · InkStack", section 1.2.1,
+ * the gradients of ordinary attention).  For every batch b, head h and query row i, with the
+ * visible keys J_i of the forward pass and L = sum_i dO_i . O_i as the loss whose gradient is taken
+ * (dO given):
+ *   P_ij = softmax_j(scale * q_i . k_j)                  (safe softmax, as the forward)
+ *   O_i  = sum_j P_ij v_j,   LSE_i = m_i + log l_i
+ *   D_i  = dO_i . O_i                                     (equal to sum_j P_ij dP_ij)
+ *   dP_ij = dO_i . v_j,      dS_ij = P_ij (dP_ij - D_i)
+ *   dV_j += P_ij dO_i,       dQ_i = scale sum_j dS_ij k_j,   dK_j += scale dS_ij q_i
+ * One work item is one head; its rows run in order, accumulating dK and dV.
+ */
+typedef struct {
+    const void *q, *k, *v, *dout;
+    int dtype;
+    int64_t B, H, N, d;
+    double scale;
+    int causal;
+    double *dq, *dk, *dv;     /* [B*H, N, d] */
+    double *o, *lse, *delta;  /* [B*H, N, d], [B*H, N], [B*H, N] */
+    int64_t next;
+    pthread_mutex_t mu;
+    int failed;
+} bwd_job_t;
+
+static void bwd_head(bwd_job_t* jb, int64_t bh, double* Q, double* K, double* V, double* dO,
+                     double* p, double* dp) {
+    job_t dec; /* only the decoding fields are used */
+    memset(&dec, 0, sizeof dec);
+    dec.dtype = jb->dtype;
+    const int64_t N = jb->N, d = jb->d, off = bh * N * d;
+    load_elems(&dec, jb->q, off, N * d, Q);
+    load_elems(&dec, jb->k, off, N * d, K);
+    load_elems(&dec, jb->v, off, N * d, V);
+    load_elems(&dec, jb->dout, off, N * d, dO);
+    double* dq = jb->dq + off;
+    double* dk = jb->dk + off;
+    double* dv = jb->dv + off;
+    for (int64_t t = 0; t < N * d; ++t) dk[t] = dv[t] = 0.0;
+    for (int64_t i = 0; i < N; ++i) {
+        const double* qi = Q + i * d;
+        const double* doi = dO + i * d;
+        const int64_t nk = jb->causal ? i + 1 : N;
+        /* forward recomputation of row i */
+        double m = -INFINITY;
+        for (int64_t j = 0; j < nk; ++j) {
+            double acc = 0.0;
+            for (int64_t t = 0; t < d; ++t) acc += qi[t] * K[j * d + t];
+            p[j] = jb->scale * acc;
+            if (p[j] > m) m = p[j];
+        }
+        double l = 0.0;
+        for (int64_t j = 0; j < nk; ++j) {
+            p[j] = exp(p[j] - m);
+            l += p[j];
+        }
+        for (int64_t j = 0; j < nk; ++j) p[j] /= l;
+        double* oi = jb->o + (bh * N + i) * d;
+        for (int64_t t = 0; t < d; ++t) oi[t] = 0.0;
+        for (int64_t j = 0; j < nk; ++j)
+            for (int64_t t = 0; t < d; ++t) oi[t] += p[j] * V[j * d + t];
+        jb->lse[bh * N + i] = m + log(l);
+        double D = 0.0;
+#if ORACLE_MUTATION == 13
+        (void)oi; /* planted: D_i dropped */
+#else
+        for (int64_t t = 0; t < d; ++t) D += doi[t] * oi[t];
+#endif
+        jb->delta[bh * N + i] = D;
+        /* dP, dS and the three gradients */
+        for (int64_t j = 0; j < nk; ++j) {
+            double acc = 0.0;
+            for (int64_t t = 0; t < d; ++t) acc += doi[t] * V[j * d + t];
+            dp[j] = acc;
+        }
+        double* dqi = dq + i * d;
+        for (int64_t t = 0; t < d; ++t) dqi[t] = 0.0;
+        for (int64_t j = 0; j < nk; ++j) {
+#if ORACLE_MUTATION == 14
+            const double ds = dp[j] - D; /* planted: P factor dropped */
+#else
+            const double ds = p[j] * (dp[j] - D);
+#endif
+            for (int64_t t = 0; t < d; ++t) {
+                dqi[t] += jb->scale * ds * K[j * d + t];
+#if ORACLE_MUTATION == 12
+                dk[j * d + t] += ds * qi[t]; /* planted: scale dropped from dK */
+#else
+                dk[j * d + t] += jb->scale * ds * qi[t];
+#endif
+#if ORACLE_MUTATION == 15
+                dv[j * d + t] += ds * doi[t]; /* planted: dS in place of P */
+#else
+                dv[j * d + t] += p[j] * doi[t];
+#endif
+            }
+        }
+    }
+}
+
+static void* bwd_worker(void* arg) {
+    bwd_job_t* jb = (bwd_job_t*)arg;
+    const int64_t N = jb->N, d = jb->d;
+    double* buf = (double*)malloc((size_t)(4 * N * d + 2 * N) * sizeof(double));
+    if (!buf) {
+        pthread_mutex_lock(&jb->mu);
+        jb->failed = 1;
+        pthread_mutex_unlock(&jb->mu);
+        return NULL;
+    }
+    for (;;) {
+        pthread_mutex_lock(&jb->mu);
+        int64_t bh = jb->next++;
+        pthread_mutex_unlock(&jb->mu);
+        if (bh >= jb->B * jb->H) break;
+        bwd_head(jb, bh, buf, buf + N * d, buf + 2 * N * d, buf + 3 * N * d, buf + 4 * N * d,
+                 buf + 4 * N * d + N);
+    }
+    free(buf);
+    return NULL;
+}
+
+/*
+ * Gradients dq, dk, dv [B, H, N, d] of L = sum(O * dO) for attention over q, k, v [B, H, N, d]
+ * (dtype as oracle_attention_fwd: bf16 bits or fp64; fp8 is not a backward operand type), plus
+ * the recomputed o [B, H, N, d], lse [B, H, N] and delta D [B, H, N].  Returns 0, -1 on bad
+ * arguments, -2 if memory ran out.
+ */
+int oracle_attention_bwd(const void* q, const void* k, const void* v, const void* dout, int dtype,
+                         int64_t B, int64_t H, int64_t N, int64_t d, double scale, int causal,
+                         double* dq, double* dk, double* dv, double* o, double* lse,
+                         double* delta, int nthreads) {
+    if (!q || !k || !v || !dout || !dq || !dk || !dv || !o || !lse || !delta) return -1;
+    if (B < 1 || H < 1 || N < 1 || d < 1) return -1;
+    if (dtype != OR_BF16 && dtype != OR_F64) return -1;
+    bwd_job_t jb;
+    memset(&jb, 0, sizeof jb);
+    jb.q = q;
+    jb.k = k;
+    jb.v = v;
+    jb.dout = dout;
+    jb.dtype = dtype;
+    jb.B = B;
+    jb.H = H;
+    jb.N = N;
+    jb.d = d;
+    jb.scale = scale;
+    jb.causal = causal;
+    jb.dq = dq;
+    jb.dk = dk;
+    jb.dv = dv;
+    jb.o = o;
+    jb.lse = lse;
+    jb.delta = delta;
+    pthread_mutex_init(&jb.mu, NULL);
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > B * H) nthreads = (int)(B * H);
+    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    if (!th) return -2;
+    int started = 0;
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&th[t], NULL, bwd_worker, &jb) != 0) break;
+        ++started;
+    }
+    bwd_worker(&jb);
+    for (int t = 1; t <= started; ++t) pthread_join(th[t], NULL);
+    free(th);
+    pthread_mutex_destroy(&jb.mu);
+    return jb.failed ? -2 : 0;
+}
+
 int oracle_mutation_id(void) { return ORACLE_MUTATION; }

@@ -62,6 +62,10 @@ class Oracle:
                       ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                       ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        bw = lib.oracle_attention_bwd
+        bw.restype = ctypes.c_int
+        bw.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] + [ctypes.c_int64] * 4 + [
+            ctypes.c_double, ctypes.c_int] + [ctypes.c_void_p] * 6 + [ctypes.c_int]
         lib.oracle_decode_bf16_array.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
         lib.oracle_decode_e4m3_array.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
         lib.oracle_mutation_id.restype = ctypes.c_int
@@ -128,6 +132,30 @@ class Oracle:
         if rc != 0:
             raise RuntimeError(f"oracle_attention_fwd_blockscaled failed with code {rc}")
         return o, lse
+
+    def attention_bwd(self, q, k, v, dout, scale: float, causal: bool = False,
+                      dtype: str = "f64", threads: int | None = None):
+        """Gradients of L = sum(O * dout): returns dict of fp64 arrays dq, dk, dv [B,H,N,d] and
+        the recomputed o [B,H,N,d], lse [B,H,N], delta [B,H,N] (D_i = dO_i . O_i)."""
+        if dtype not in ("f64", "bf16"):
+            raise ValueError("the backward takes bf16 or f64 operands")
+        q, k, v = self._operands(q, k, v, dtype)
+        dout = np.ascontiguousarray(dout)
+        if dout.shape != q.shape or dout.dtype != q.dtype:
+            raise ValueError("dout must match q in shape and dtype")
+        B, H, N, d = q.shape
+        out = {n: np.empty((B, H, N, d)) for n in ("dq", "dk", "dv", "o")}
+        out["lse"] = np.empty((B, H, N))
+        out["delta"] = np.empty((B, H, N))
+        rc = self._lib.oracle_attention_bwd(
+            q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data, DTYPE_CODES[dtype],
+            B, H, N, d, float(scale), int(bool(causal)), out["dq"].ctypes.data,
+            out["dk"].ctypes.data, out["dv"].ctypes.data, out["o"].ctypes.data,
+            out["lse"].ctypes.data, out["delta"].ctypes.data,
+            int(threads or os.cpu_count() or 1))
+        if rc != 0:
+            raise RuntimeError(f"oracle_attention_bwd failed with code {rc}")
+        return out
 
     def attention_fwd(self, q, k, v, scale: float, causal: bool = False, dtype: str = "f64",
                       descale=(1.0, 1.0, 1.0), rows=None, threads: int | None = None):

@@ -286,3 +286,99 @@ def pin_uniform_block_descales_equal_per_tensor(orc):
         ot, lt = orc.attention_fwd(raw[0], raw[1], raw[2], 0.3, True, "e4m3", (dq, dk, dv))
         np.testing.assert_allclose(ob, ot, rtol=1e-12, atol=1e-12)
         np.testing.assert_allclose(lb, lt, rtol=1e-12, atol=1e-12)
+
+
+def _torch_grads(q, k, v, dout, scale, causal):
+    """Reference gradients from torch autograd in fp64 (a library routine)."""
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    s = scale * tq @ tk.transpose(-1, -2)
+    if causal:
+        n = s.shape[-1]
+        s = s.masked_fill(~torch.ones(n, n, dtype=torch.bool).tril(), float("-inf"))
+    o = torch.softmax(s, dim=-1) @ tv
+    o.backward(torch.tensor(dout, dtype=torch.float64))
+    return o.detach().numpy(), tq.grad.numpy(), tk.grad.numpy(), tv.grad.numpy()
+
+
+@pin
+def pin_backward_matches_torch_autograd(orc):
+    """dQ, dK, dV of L = sum(O * dO) equal torch autograd's on small shapes ("FlashAttention ·
+    InkStack", section 1.2.1: dV = P^T dO, dS = P (dP - D), dQ = scale dS K, dK = scale dS^T Q)."""
+    rng = np.random.default_rng(40)
+    for causal in (False, True):
+        for (B, H, N, d) in [(1, 1, 1, 2), (1, 2, 7, 4), (2, 1, 33, 8)]:
+            q, k, v, do = rng.standard_normal((4, B, H, N, d))
+            g = orc.attention_bwd(q, k, v, do, 0.6, causal)
+            o, dq, dk, dv = _torch_grads(q, k, v, do, 0.6, causal)
+            for got, want in ((g["o"], o), (g["dq"], dq), (g["dk"], dk), (g["dv"], dv)):
+                np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+
+
+@pin
+def pin_backward_finite_differences(orc):
+    """Central differences of L = sum(O * dO) through the oracle's own forward agree with its
+    gradients (no library involved)."""
+    rng = np.random.default_rng(41)
+    B, H, N, d = 1, 1, 6, 3
+    q, k, v, do = rng.standard_normal((4, B, H, N, d))
+    g = orc.attention_bwd(q, k, v, do, 0.9, True)
+
+    def loss(q_, k_, v_):
+        o, _ = orc.attention_fwd(q_, k_, v_, 0.9, True)
+        return float((o * do).sum())
+
+    h = 1e-6
+    for name, arr in (("dq", q), ("dk", k), ("dv", v)):
+        for idx in [(0, 0, 0, 0), (0, 0, 3, 1), (0, 0, N - 1, d - 1)]:
+            plus, minus = arr.copy(), arr.copy()
+            plus[idx] += h
+            minus[idx] -= h
+            args_p = [plus if a is arr else a for a in (q, k, v)]
+            args_m = [minus if a is arr else a for a in (q, k, v)]
+            fd = (loss(*args_p) - loss(*args_m)) / (2 * h)
+            assert abs(fd - g[name][idx]) < 1e-7, (name, idx, fd, g[name][idx])
+
+
+@pin
+def pin_backward_delta_identity(orc):
+    """D_i = dO_i . O_i equals sum_j P_ij dP_ij with dP = dO V^T ("FlashAttention · InkStack",
+    section 1.2.1), P taken from scipy's softmax."""
+    rng = np.random.default_rng(42)
+    B, H, N, d = 1, 2, 20, 5
+    q, k, v, do = rng.standard_normal((4, B, H, N, d))
+    g = orc.attention_bwd(q, k, v, do, 0.4, False)
+    for h in range(H):
+        p = sps.softmax(0.4 * q[0, h] @ k[0, h].T, axis=1)
+        dp = do[0, h] @ v[0, h].T
+        np.testing.assert_allclose(g["delta"][0, h], (p * dp).sum(axis=1), rtol=0, atol=1e-12)
+
+
+@pin
+def pin_backward_causal_last_key(orc):
+    """Under the causal mask only the last query sees the last key: dV_{N-1} = P_{N-1,N-1} dO_{N-1}
+    and dK_{N-1} = scale dS_{N-1,N-1} q_{N-1}."""
+    rng = np.random.default_rng(43)
+    B, H, N, d = 1, 1, 9, 4
+    q, k, v, do = rng.standard_normal((4, B, H, N, d))
+    g = orc.attention_bwd(q, k, v, do, 0.5, True)
+    x = 0.5 * q[0, 0, -1] @ k[0, 0].T
+    p = sps.softmax(x)
+    dp = do[0, 0, -1] @ v[0, 0].T
+    ds = p * (dp - (p * dp).sum())
+    np.testing.assert_allclose(g["dv"][0, 0, -1], p[-1] * do[0, 0, -1], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(g["dk"][0, 0, -1], 0.5 * ds[-1] * q[0, 0, -1], rtol=0, atol=1e-12)
+
+
+@pin
+def pin_backward_key_shift_invariance(orc):
+    """K <- K + u shifts every score of row i by the same amount, so P, dV and dQ are unchanged
+    (the rows of dS sum to zero)."""
+    rng = np.random.default_rng(44)
+    B, H, N, d = 1, 1, 15, 6
+    q, k, v, do = rng.standard_normal((4, B, H, N, d))
+    u = rng.standard_normal(d)
+    for causal in (False, True):
+        g0 = orc.attention_bwd(q, k, v, do, 0.7, causal)
+        g1 = orc.attention_bwd(q, k + u, v, do, 0.7, causal)
+        np.testing.assert_allclose(g1["dq"], g0["dq"], rtol=0, atol=1e-11)
+        np.testing.assert_allclose(g1["dv"], g0["dv"], rtol=0, atol=1e-11)

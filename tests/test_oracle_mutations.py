@@ -3,7 +3,8 @@
 The oracle's C source carries a handful of deliberate mistakes behind ``ORACLE_MUTATION``
 (a dropped scale, an off-by-one causal mask, a dropped max in the LSE, the wrong operand in P.V,
 a dropped normalisation, a shifted value index, an ignored value descale, a wrong e4m3 exponent
-bias, a base-2 LSE, two block-descale indexing slips).  The default build has none.
+bias, a base-2 LSE, two block-descale indexing slips,
+four backward slips).  The default build has none.
 """
 import os
 
@@ -24,6 +25,10 @@ MUTATIONS = {
     9: "LSE in base 2",
     10: "query block descale read from the first head",
     11: "key block descale applied to the values",
+    12: "backward: scale dropped from dK",
+    13: "backward: D dropped",
+    14: "backward: P factor of dS dropped",
+    15: "backward: dS used in place of P for dV",
 }
 
 

@@ -50,3 +50,20 @@ def test_threads_do_not_change_results(orc):
     b = orc.attention_fwd(q, k, v, 0.3, True, threads=max(2, os.cpu_count() or 2))
     np.testing.assert_array_equal(a[0], b[0])
     np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_backward_bf16_inputs_match_f64_on_decoded_values(orc):
+    from workloads import random_bwd_inputs
+
+    inp = random_bwd_inputs(1, 2, 40, 16, seed=5)
+    g16 = orc.attention_bwd(*(inp.raw(n) for n in ("q", "k", "v", "do")), 0.25, True, "bf16")
+    g64 = orc.attention_bwd(*(getattr(inp, n).double().numpy() for n in ("q", "k", "v", "do")),
+                            0.25, True)
+    for key in ("dq", "dk", "dv", "o", "lse", "delta"):
+        np.testing.assert_array_equal(g16[key], g64[key])
+
+
+def test_backward_rejects_bad_arguments(orc):
+    x = np.zeros((1, 1, 4, 2), dtype=np.uint8)
+    with pytest.raises(ValueError):
+        orc.attention_bwd(x, x, x, x, 1.0, False, "e4m3")

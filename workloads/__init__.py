@@ -196,6 +196,28 @@ def blockscaled_inputs(B: int, H: int, N: int, d: int, seed: int = 0,
     return BlockScaledInputs(base.q, base.k, base.v, *ds)
 
 
+@dataclass
+class BwdInputs:
+    """Operands of the backward pass: Q, K, V and the output gradient dO, bf16 [B, H, N, d]."""
+
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    do: torch.Tensor
+
+    def raw(self, name: str):
+        return getattr(self, name).contiguous().view(torch.int16).numpy().view("uint16")
+
+
+def random_bwd_inputs(B: int, H: int, N: int, d: int, seed: int = 0) -> BwdInputs:
+    """iid N(0,1) draws for Q, K, V, then dO (in that order), rounded to bf16."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    shape = (B, H, N, d)
+    q, k, v, do = (torch.randn(shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
+                   for _ in range(4))
+    return BwdInputs(q, k, v, do)
+
+
 def make_inputs(w: Workload) -> Inputs:
     return random_inputs(w.B, w.H, w.N, w.d, w.dtype, w.seed, w.q_mult)
 
