@@ -463,6 +463,67 @@ def run_quantize(args, w, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_backward(args, w, world, rank, local):
+    """Time the attention backward (fa_bwd: D, dK/dV and dQ kernels) on the workload's shape,
+    with O and LSE from the forward.  Work counted: 10·B·H·N²·d flop (halved causal), the five
+    N²d products of the backward (2.5x the forward's)."""
+    import torch
+
+    import exact_attention_13_gb300 as ea
+    from workloads import random_bwd_inputs
+
+    if w.dtype != "bf16":
+        raise SystemExit("the backward takes bf16 operands")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    inp = random_bwd_inputs(w.B, w.H, w.N, w.d, w.seed)
+    q, k, v, do = (getattr(inp, n).to(dev) for n in ("q", "k", "v", "do"))
+    o, lse = ea.fwd(q, k, v, causal=w.causal)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    ws = torch.empty(ea.bwd_workspace_bytes(w.B, w.H, w.N), dtype=torch.uint8, device=dev)
+
+    def step():
+        ea.bwd(q, k, v, o, lse, do, causal=w.causal, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize()
+    ms = max_over_ranks(start.elapsed_time(end) / args.steps, world, dev)
+    assert ea.device_status() == 0, "device wait timed out during the bench"
+    if rank != 0:
+        return
+    flops = 2.5 * w.flops
+    tf = flops / (ms * 1e-3) / 1e12
+    pk = peaks()
+    line = {
+        "metric": "attention bwd TFLOPS (10·B·H·N²·d, halved causal; 1 GPU, device-timed)",
+        "value": tf * world, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "shape": w.describe(), "op": "backward"},
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": pk["bf16"], "unit": "TFLOP/s",
+                     "frac": tf / pk["bf16"], "traffic": None,
+                     "peak_kind": f"{pk['source']} cuBLAS bf16 burst",
+                     "kernel": "exattn::bwd_dkdv_kernel + bwd_dq_kernel + bwd_delta_kernel"},
+        "clocks": clk.summary(),
+        "gpu_launches": 3 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -477,8 +538,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fp8-pv", default="e4m3", choices=["e4m3", "f16"],
                     help="fp8 operands: precision of the P V product")
-    ap.add_argument("--op", default="attention", choices=["attention", "quantize"],
-                    help="attention forward (default) or the fp8 block quantiser alone")
+    ap.add_argument("--op", default="attention", choices=["attention", "quantize", "backward"],
+                    help="attention forward (default), the fp8 block quantiser alone, or the "
+                         "attention backward")
     ap.add_argument("--hadamard", action="store_true",
                     help="--op quantize: apply the incoherent (Hadamard) transform")
     ap.add_argument("--traffic-bytes", type=float, default=None,
@@ -495,6 +557,8 @@ def main():
     world, rank, local = init_dist()
     if args.op == "quantize":
         run_quantize(args, w, world, rank, local)
+    elif args.op == "backward":
+        run_backward(args, w, world, rank, local)
     else:
         run_ours(args, w, world, rank, local)
     if world > 1:

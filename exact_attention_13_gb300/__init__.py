@@ -57,6 +57,9 @@ SIGNATURES = {
                                           _c.c_void_p, _c.c_void_p]),
     "fa_quantize_e4m3": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_int,
                                     _c.c_int, _c.c_int, _c.c_void_p, _c.c_int, _c.c_void_p]),
+    "fa_bwd": (_c.c_int, [_c.c_void_p] * 5 + [_c.c_void_p] * 4 + [_c.c_int] * 4 + [
+        _c.c_float, _c.c_int, _c.c_void_p, _c.c_size_t, _c.c_void_p, _c.c_void_p]),
+    "fa_bwd_workspace_bytes": (_c.c_size_t, [_c.c_int, _c.c_int, _c.c_int]),
     "fa_device_status": (_c.c_int, [_c.c_int, _c.POINTER(_c.c_int)]),
     "fa_status_string": (_c.c_char_p, [_c.c_int]),
     "fa_version": (_c.c_int, []),
@@ -318,6 +321,50 @@ def fwd_fp8_blockscaled(q, k, v, dq_blk, dk_blk, dv_blk, causal: bool = False,
                                     FA_DTYPE_FP8_E4M3_PV16 if pv16 else FA_DTYPE_FP8_E4M3)
     _check(rc, "fa_fwd_fp8_blockscaled")
     return out, lse
+
+
+def fa_bwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, do_ptr, dq_ptr, dk_ptr, dv_ptr, B, H, N, d,
+           scale, causal, workspace_ptr, workspace_bytes, status_ptr=None, stream=None) -> int:
+    return lib().fa_bwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, do_ptr, dq_ptr, dk_ptr, dv_ptr, B, H,
+                        N, d, scale, int(causal), workspace_ptr, int(workspace_bytes), status_ptr,
+                        stream)
+
+
+def bwd_workspace_bytes(B: int, H: int, N: int) -> int:
+    return int(lib().fa_bwd_workspace_bytes(B, H, N))
+
+
+def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, dq=None,
+        dk=None, dv=None, workspace=None, status=None):
+    """Attention backward on bf16 CUDA tensors [B, H, N, d]: o and lse are the forward's outputs
+    for q, k, v; dout is dL/dO.  Returns (dq, dk, dv), bf16."""
+    import torch
+
+    for t in (q, k, v, o, dout):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("q, k, v, o, dout must be contiguous bf16 CUDA tensors")
+        if t.shape != q.shape:
+            raise ValueError("q, k, v, o, dout must share one [B, H, N, d] shape")
+    B, H, N, d = q.shape
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    need = bwd_workspace_bytes(B, H, N)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    st = status.data_ptr() if status is not None else None
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    with torch.cuda.device(q.device):
+        rc = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                    dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+                    float(scale), causal, workspace.data_ptr(),
+                    workspace.numel() * workspace.element_size(), st, stream)
+    _check(rc, "fa_bwd")
+    return dq, dk, dv
 
 
 def debug_exp2(x, mode: int):

@@ -10,7 +10,7 @@ CSRC = os.path.join(PKG, "csrc")
 ROOT = os.path.dirname(PKG)
 LIB_PATH = os.path.join(PKG, "libexattn.so")
 SOURCES = [os.path.join(CSRC, "fa_api.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("fa_fwd_kernel.cuh", "fa_quant.cuh", "sm103_ptx.cuh")] + [
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("fa_fwd_kernel.cuh", "fa_quant.cuh", "fa_bwd_kernel.cuh", "sm103_ptx.cuh")] + [
     os.path.join(ROOT, "include", "exact_attention.h")]
 
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-lineinfo",

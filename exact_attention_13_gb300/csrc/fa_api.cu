@@ -11,6 +11,7 @@
 #include "../../include/exact_attention.h"
 #include "fa_fwd_kernel.cuh"
 #include "fa_quant.cuh"
+#include "fa_bwd_kernel.cuh"
 
 namespace exattn {
 namespace {
@@ -197,6 +198,66 @@ int launch_combine(const float* o_part, const float* lse_part, void* o, float* l
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Bytes of the backward's scratch: D [B*H*N] fp32, rounded up to 256.
+size_t bwd_workspace_bytes(int B, int H, int N) {
+  const size_t bytes = static_cast<size_t>(B) * H * N * 4;
+  return (bytes + 255) / 256 * 256;
+}
+
+template <typename K>
+bool set_smem_once(K kern, int bytes, int dev, std::atomic<uint64_t>& done) {
+  if (done.load(std::memory_order_acquire) & (1ull << dev)) return true;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+      cudaSuccess)
+    return false;
+  done.fetch_or(1ull << dev, std::memory_order_acq_rel);
+  return true;
+}
+
+// Backward: D, then dK/dV, then dQ, all on `stream`.
+template <int D, bool CAUSAL>
+int launch_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+               const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, float scale,
+               float* delta, int* status, cudaStream_t stream) {
+  const int bh = B * H;
+  CUtensorMap mq, mk, mv, mdo;
+  if (!encode_operand_map(&mq, q, 2, D, N, bh) || !encode_operand_map(&mk, k, 2, D, N, bh) ||
+      !encode_operand_map(&mv, v, 2, D, N, bh) || !encode_operand_map(&mdo, dout, 2, D, N, bh))
+    return FA_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  BwdArgs a;
+  a.lse = lse;
+  a.delta = delta;
+  a.status = status ? status : library_status_ptr(dev);
+  if (!a.status) return FA_ERR_CUDA;
+  a.n = N;
+  a.c = scale * 1.4426950408889634f;
+  a.scale = scale;
+  const long long rows = static_cast<long long>(bh) * N;
+  bwd_delta_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), delta, rows);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  constexpr int smem = bwd_smem_bytes<D>();
+  static_assert(smem <= 227 * 1024, "shared memory per CTA");
+  constexpr int smem_request = smem > 120 * 1024 ? smem : 120 * 1024;
+  static std::atomic<uint64_t> done_kv{0}, done_q{0};
+  auto kkv = bwd_dkdv_kernel<D, CAUSAL>;
+  auto kq = bwd_dq_kernel<D, CAUSAL>;
+  if (!set_smem_once(kkv, smem_request, dev, done_kv) || !set_smem_once(kq, smem_request, dev, done_q))
+    return FA_ERR_CUDA;
+  const unsigned nblk = static_cast<unsigned>((N + kTileRows - 1) / kTileRows);
+  const dim3 grid = CAUSAL ? dim3(static_cast<unsigned>(bh), nblk) : dim3(nblk, static_cast<unsigned>(bh));
+  a.g0 = static_cast<__nv_bfloat16*>(dk);
+  a.g1 = static_cast<__nv_bfloat16*>(dv);
+  kkv<<<grid, kBwdThreads, smem_request, stream>>>(mq, mk, mv, mdo, a);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  a.g0 = static_cast<__nv_bfloat16*>(dq);
+  a.g1 = nullptr;
+  kq<<<grid, kBwdThreads, smem_request, stream>>>(mq, mk, mv, mdo, a);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 __global__ void exp2_probe_kernel(const float* x, float* y, long long n, int mode) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x)
@@ -325,6 +386,41 @@ int fa_fwd_fp8_blockscaled(const void* q, const void* k, const void* v, void* o,
   const BlockScales bs{descale_q_blk, descale_k_blk, descale_v_blk};
   return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, &opts, num_splits,
                   workspace, workspace_bytes, stream, &bs);
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int N) {
+  if (B < 1 || H < 1 || N < 1) return 0;
+  return bwd_workspace_bytes(B, H, N);
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+           const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+           float scale, int causal, void* workspace, size_t workspace_bytes, int* dev_status,
+           void* stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace)
+    return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H > 65535) return FA_ERR_UNSUPPORTED;
+  if ((N + kTileRows - 1) / kTileRows > 65535 || N > 0x7FFFFFFF - kTileRows)
+    return FA_ERR_UNSUPPORTED;
+  if (workspace_bytes < bwd_workspace_bytes(B, H, N)) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(lse, 4) || !aligned(workspace, 16) || (dev_status && !aligned(dev_status, 4)))
+    return FA_ERR_MISALIGNED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* delta = static_cast<float*>(workspace);
+  if (d == 64)
+    return causal ? launch_bwd<64, true>(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, scale, delta,
+                                         dev_status, s)
+                  : launch_bwd<64, false>(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, scale,
+                                          delta, dev_status, s);
+  return causal ? launch_bwd<128, true>(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, scale, delta,
+                                        dev_status, s)
+                : launch_bwd<128, false>(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, scale, delta,
+                                         dev_status, s);
 }
 
 int fa_quantize_e4m3(const void* x, void* codes, float* descales, int B, int H, int N, int d,

@@ -1,0 +1,577 @@
+// fa_bwd_kernel.cuh -- attention backward for sm_103a (tcgen05 + TMEM + TMA), bf16 operands.
+//
+// Gradients of exact attention ("FlashAttention · InkStack", section 1.2 "反向传播"): with P
+// recomputed from the forward pass's log-sum-exp (P_ij = exp(scale q_i.k_j - LSE_i), the
+// recomputation of section 1.2.2) and D_i = rowsum(dO_i * O_i):
+//
+//   dV_j = sum_i P_ij^T dO_i          dP_ij = dO_i V_j^T          dS_ij = P_ij * (dP_ij - D_i)
+//   dK_j = scale sum_i dS_ij^T Q_i    dQ_i  = scale sum_j dS_ij K_j
+//
+// Three launches:
+//   bwd_delta_kernel   D_i = dO_i . O_i (fp32), one warp per row;
+//   bwd_dkdv_kernel    one CTA per (head, 128-key block j): K_j and V_j stay in shared memory,
+//                      the query blocks i stream through a two-stage ring; per i the tensor core
+//                      computes S^T = K_j Q_i^T and dP^T = V_j dO_i^T into TMEM, the softmax warps
+//                      turn them into P^T and dS^T (bf16, written back over S^T and dP^T), and the
+//                      tensor core accumulates dV_j += P^T dO_i and dK_j += dS^T Q_i in TMEM;
+//   bwd_dq_kernel      one CTA per (head, 128-query block i): Q_i and dO_i stay, the key blocks
+//                      stream; per j S = Q_i K_j^T and dP = dO_i V_j^T, the softmax warps form dS,
+//                      and dQ_i += dS K_j accumulates in TMEM.
+// Splitting dQ from dK/dV recomputes S and dP once more (7 products instead of 5) but needs no
+// atomics and no fp32 dQ accumulator in global memory.
+//
+// The MMAs are the forward kernel's: S-type products have both operands K-major in shared memory
+// (128-byte swizzled TMA tiles), the accumulating products take their A operand (P^T, dS^T or dS,
+// bf16) from TMEM and their B operand MN-major from the same tiles.  Warp roles (384 threads):
+// warps 0-7 one half-row of S each (warp w: TMEM lanes 32 (w % 4) .., columns 64 (w / 4) ..),
+// warp 8 TMA, warp 9 MMA issue and TMEM owner, warp 10 (dK/dV only) stages LSE and D of each query
+// block in shared memory.  Every wait is bounded as in the forward kernel.
+#pragma once
+
+#include "fa_fwd_kernel.cuh"
+
+namespace exattn {
+
+constexpr int kBwdThreads = 384;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdGeo {
+  static constexpr int kBoxes = D / 64;                     // 64-column (128-byte) TMA boxes
+  static constexpr int kTileBytes = kTileRows * D * 2;      // one 128-row bf16 tile
+  static constexpr int kKSteps = D / 16;                    // MMAs per S-type product
+  static constexpr uint32_t kIdescS = instr_desc(128, 128, 1, false, false);
+  static constexpr uint32_t kIdescAcc = instr_desc(128, D, 1, false, true);
+  static constexpr int kHalfCols = D / 2;                   // output columns per thread
+};
+
+struct BwdArgs {
+  __nv_bfloat16* g0;      // dkdv: dK out; dq: dQ out            [BH, N, d]
+  __nv_bfloat16* g1;      // dkdv: dV out                         [BH, N, d]
+  const float* lse;       // forward log-sum-exp (natural log)    [BH, N]
+  const float* delta;     // D                                    [BH, N]
+  int* status;
+  int n;
+  float c;                // scale * log2(e)
+  float scale;
+};
+
+struct BwdCtrl {
+  uint64_t fix_full;      // the CTA's fixed pair of tiles (dK/dV: K_j, V_j; dQ: Q_i, dO_i)
+  uint64_t ring_full[2];  // streamed pair (dK/dV: Q_i, dO_i; dQ: K_j, V_j)
+  uint64_t ring_empty[2];
+  uint64_t vec_full[2];   // LSE and D of the query block (dK/dV)
+  uint64_t s_full;        // both S-type products of the step are in TMEM
+  uint64_t p_full;        // P / dS written back (eight warps)
+  uint64_t o_full;        // the last accumulating product is done
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  float lse2[2][kTileRows];   // LSE * log2(e) of the stage's 128 queries
+  float dlt[2][kTileRows];    // D of the stage's 128 queries
+};
+
+// two fixed tiles + two ring stages of two tiles + the control block
+template <int D>
+constexpr int bwd_smem_bytes() {
+  return 6 * BwdGeo<D>::kTileBytes + static_cast<int>(sizeof(BwdCtrl)) + 1024;
+}
+
+// D_i = sum_t dO_it O_it in fp32, one warp per row.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
+                                                        const __nv_bfloat16* __restrict__ dout,
+                                                        float* __restrict__ delta, long long rows) {
+  constexpr int kPer = D / 32;
+  const long long row = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+  if (row >= rows) return;
+  const int lane = threadIdx.x % 32;
+  const __nv_bfloat16* a = o + row * D + lane * kPer;
+  const __nv_bfloat16* b = dout + row * D + lane * kPer;
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < kPer; i += 2) {
+    const uint32_t wa = *reinterpret_cast<const uint32_t*>(a + i);
+    const uint32_t wb = *reinterpret_cast<const uint32_t*>(b + i);
+    acc = fmaf(__uint_as_float(wa << 16), __uint_as_float(wb << 16), acc);
+    acc = fmaf(__uint_as_float(wa & 0xFFFF0000u), __uint_as_float(wb & 0xFFFF0000u), acc);
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) delta[row] = acc;
+}
+
+// TMEM column of the A operand for k-step kb of an accumulating product: the softmax warps of
+// column half 0 write their 64 bf16 values to columns [0, 32), those of half 1 to [64, 96), each
+// inside the S columns it read itself (so no warp overwrites S another warp has not read yet).
+__device__ __forceinline__ uint32_t p_col(int kb) { return kb < 4 ? kb * 8 : 64 + (kb - 4) * 8; }
+
+// S-type product into TMEM columns [col, col + 128): A and B both 128 x D K-major tiles.
+template <int D>
+__device__ __forceinline__ void mma_s_type(uint32_t tmem_d, uint32_t a_tile, uint32_t b_tile) {
+  using G = BwdGeo<D>;
+#pragma unroll
+  for (int kb = 0; kb < G::kKSteps; ++kb) {
+    const uint32_t off = (kb * 32 / 128) * kTileRows * 128 + (kb * 32) % 128;
+    mma_f16_ss(tmem_d, smem_desc(a_tile + off, 16, 1024, kSwizzle128B),
+               smem_desc(b_tile + off, 16, 1024, kSwizzle128B), G::kIdescS, kb > 0);
+  }
+}
+
+// Accumulating product D += A (128 x 128 bf16 from TMEM) * B (128 x D tile, MN-major).
+template <int D>
+__device__ __forceinline__ void mma_acc(uint32_t tmem_d, uint32_t tmem_a, uint32_t b_tile,
+                                        bool accumulate) {
+  using G = BwdGeo<D>;
+#pragma unroll
+  for (int kb = 0; kb < 8; ++kb)
+    mma_f16_ts(tmem_d, tmem_a + p_col(kb),
+               smem_desc(b_tile + kb * 16 * 128, kTileRows * 128, 1024, kSwizzle128B),
+               G::kIdescAcc, (accumulate || kb > 0) ? 1u : 0u);
+}
+
+// Half-row softmax step shared by both kernels: 64 scores s and 64 dP values of this thread's
+// row, turned into P (bf16, written over the S columns) and dS = P (dP - D) (bf16, over the dP
+// columns).  lse2/dlt give each column's LSE * log2(e) and D (dK/dV kernel: per query column;
+// dQ kernel: the row's own values repeated); `visible` says which columns are unmasked.
+template <typename LseFn, typename DltFn, typename VisFn>
+__device__ __forceinline__ void softmax_half(uint32_t t_s, uint32_t t_dp, float c, LseFn lse2,
+                                             DltFn dlt, VisFn visible, bool any_masked) {
+  float s[64], dp[64];
+  {
+    uint32_t r0[32], r1[32], r2[32], r3[32];
+    tmem_ld32(t_s, r0);
+    tmem_ld32(t_s + 32, r1);
+    tmem_ld32(t_dp, r2);
+    tmem_ld32(t_dp + 32, r3);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      s[i] = __uint_as_float(r0[i]);
+      s[32 + i] = __uint_as_float(r1[i]);
+      dp[i] = __uint_as_float(r2[i]);
+      dp[32 + i] = __uint_as_float(r3[i]);
+    }
+  }
+  uint32_t pp[32], pd[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    float p0 = ex2_mufu(fmaf(s[2 * i], c, -lse2(2 * i)));
+    float p1 = ex2_mufu(fmaf(s[2 * i + 1], c, -lse2(2 * i + 1)));
+    if (any_masked) {
+      p0 = visible(2 * i) ? p0 : 0.f;
+      p1 = visible(2 * i + 1) ? p1 : 0.f;
+    }
+    const float d0 = p0 * (dp[2 * i] - dlt(2 * i));
+    const float d1 = p1 * (dp[2 * i + 1] - dlt(2 * i + 1));
+    pp[i] = pack_bf16x2(p0, p1);
+    pd[i] = pack_bf16x2(d0, d1);
+  }
+  tmem_st32(t_s, pp);
+  tmem_st32(t_dp, pd);
+  tmem_st_wait();
+}
+
+// ------------------------------------------------------------------------------------------
+// dK, dV: one CTA per (head, key block).  Grid (key blocks, BH); causal: (BH, key blocks) with
+// the key blocks in increasing order, i.e. the CTAs with the most query blocks first.
+// ------------------------------------------------------------------------------------------
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                    const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
+                    const BwdArgs args) {
+  using G = BwdGeo<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* s_k = smem;
+  uint8_t* s_v = smem + G::kTileBytes;
+  uint8_t* s_ring = smem + 2 * G::kTileBytes;  // stage s: Q at 2s, dO at 2s + 1 (tiles)
+  BwdCtrl* ctl = reinterpret_cast<BwdCtrl*>(smem + 6 * G::kTileBytes);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int n = args.n;
+  const int bh = CAUSAL ? blockIdx.x : blockIdx.y;
+  const int jblk = CAUSAL ? blockIdx.y : blockIdx.x;
+  const int nblk = (n + kTileRows - 1) / kTileRows;
+  const int i0 = CAUSAL ? jblk : 0;   // first query block that sees this key block
+  const int nq = nblk - i0;           // query blocks visited (>= 1)
+  int* const status = args.status;
+
+  if (warp == 9) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), 512);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&ctl->fix_full), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&ctl->ring_full[s]), 1);
+      mbar_init(smem_u32(&ctl->ring_empty[s]), 1);
+      mbar_init(smem_u32(&ctl->vec_full[s]), 1);
+    }
+    mbar_init(smem_u32(&ctl->s_full), 1);
+    mbar_init(smem_u32(&ctl->p_full), 8);
+    mbar_init(smem_u32(&ctl->o_full), 1);
+    mbar_init(smem_u32(&ctl->drain), 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  int* abort_flag = &ctl->abort;
+
+  if (warp >= 8) {
+    regs_dec<72>();
+    if (warp == 8) {
+      // ------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        tma_prefetch_map(&map_q);
+        tma_prefetch_map(&map_k);
+        tma_prefetch_map(&map_v);
+        tma_prefetch_map(&map_do);
+        const uint32_t fb = smem_u32(&ctl->fix_full);
+        mbar_arrive_expect_tx(fb, 2 * G::kTileBytes);
+        for (int b = 0; b < G::kBoxes; ++b) {
+          tma_load_3d(smem_u32(s_k + b * kTileRows * 128), &map_k, fb, b * 64, jblk * kTileRows, bh);
+          tma_load_3d(smem_u32(s_v + b * kTileRows * 128), &map_v, fb, b * 64, jblk * kTileRows, bh);
+        }
+        bool ok = true;
+        int issued = 0;
+        for (int u = 0; u < nq && ok; ++u) {
+          const int s = u & 1;
+          if (u >= 2) {
+            ok = wait_phase(smem_u32(&ctl->ring_empty[s]), ((u >> 1) - 1) & 1, abort_flag, status);
+            if (!ok) break;
+          }
+          const uint32_t rb = smem_u32(&ctl->ring_full[s]);
+          mbar_arrive_expect_tx(rb, 2 * G::kTileBytes);
+          uint8_t* dq = s_ring + (2 * s) * G::kTileBytes;
+          uint8_t* ddo = s_ring + (2 * s + 1) * G::kTileBytes;
+          const int row = (i0 + u) * kTileRows;
+          for (int b = 0; b < G::kBoxes; ++b) {
+            tma_load_3d(smem_u32(dq + b * kTileRows * 128), &map_q, rb, b * 64, row, bh);
+            tma_load_3d(smem_u32(ddo + b * kTileRows * 128), &map_do, rb, b * 64, row, bh);
+          }
+          ++issued;
+        }
+        if (!ok) {
+          // abort: let the copies already issued land before the CTA's smem goes away
+          wait_phase(fb, 0, abort_flag, status);
+          for (int u = issued > 2 ? issued - 2 : 0; u < issued; ++u) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(smem_u32(&ctl->ring_full[u & 1]), (u >> 1) & 1) &&
+                   globaltimer_ns() - t0 < kWaitLimitNs) {
+            }
+          }
+        }
+      }
+    } else if (warp == 9) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        bool ok = wait_phase(smem_u32(&ctl->fix_full), 0, abort_flag, status);
+        tc_fence_after();
+        const uint32_t k_tile = smem_u32(s_k), v_tile = smem_u32(s_v);
+        for (int u = 0; u < nq && ok; ++u) {
+          const int s = u & 1;
+          ok = wait_phase(smem_u32(&ctl->ring_full[s]), (u >> 1) & 1, abort_flag, status);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t q_tile = smem_u32(s_ring + (2 * s) * G::kTileBytes);
+          const uint32_t do_tile = smem_u32(s_ring + (2 * s + 1) * G::kTileBytes);
+          mma_s_type<D>(tmem, k_tile, q_tile);          // S^T  = K_j Q_i^T
+          mma_s_type<D>(tmem + 128, v_tile, do_tile);   // dP^T = V_j dO_i^T
+          tc_commit(smem_u32(&ctl->s_full));
+          ok = wait_phase(smem_u32(&ctl->p_full), u & 1, abort_flag, status);
+          if (!ok) break;
+          tc_fence_after();
+          mma_acc<D>(tmem + 256, tmem, do_tile, u > 0);        // dV += P^T dO_i
+          mma_acc<D>(tmem + 384, tmem + 128, q_tile, u > 0);   // dK += dS^T Q_i
+          tc_commit(smem_u32(&ctl->ring_empty[s]));
+        }
+        if (ok) tc_commit(smem_u32(&ctl->o_full));
+        tc_commit(smem_u32(&ctl->drain));
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(smem_u32(&ctl->drain), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    } else if (warp == 10) {
+      // ------------------------------------------------------------ LSE / D stager
+      bool ok = true;
+      for (int u = 0; u < nq && ok; ++u) {
+        const int s = u & 1;
+        if (u >= 2)
+          ok = wait_phase(smem_u32(&ctl->ring_empty[s]), ((u >> 1) - 1) & 1, abort_flag, status);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        const int row0 = (i0 + u) * kTileRows;
+#pragma unroll
+        for (int q = lane; q < kTileRows; q += 32) {
+          const int row = row0 + q;
+          const size_t idx = static_cast<size_t>(bh) * n + row;
+          ctl->lse2[s][q] = row < n ? args.lse[idx] * kLog2e : 0.f;
+          ctl->dlt[s][q] = row < n ? args.delta[idx] : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->vec_full[s]));
+      }
+    }
+  } else {
+    regs_inc<216>();
+    // ------------------------------------------------------------ softmax warps
+    const int w4 = warp % 4, hc = warp / 4;
+    const int r = w4 * 32 + lane;                  // key row within the block (TMEM lane)
+    const int key = jblk * kTileRows + r;
+    const uint32_t lane_addr = static_cast<uint32_t>(w4 * 32) << 16;
+    const uint32_t t_s = tmem + lane_addr + 64 * hc;
+    const uint32_t t_dp = tmem + lane_addr + 128 + 64 * hc;
+    bool ok = true;
+    for (int u = 0; u < nq && ok; ++u) {
+      const int s = u & 1;
+      const int qblk = i0 + u;
+      ok = wait_phase(smem_u32(&ctl->vec_full[s]), (u >> 1) & 1, abort_flag, status);
+      if (ok) ok = wait_phase(smem_u32(&ctl->s_full), u & 1, abort_flag, status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const float* l2 = ctl->lse2[s] + 64 * hc;
+      const float* dl = ctl->dlt[s] + 64 * hc;
+      const int q0 = qblk * kTileRows + 64 * hc;   // first query column of this half
+      const bool any_masked = (CAUSAL && qblk == jblk) || (qblk + 1) * kTileRows > n;
+      softmax_half(
+          t_s, t_dp, args.c, [&](int q) { return l2[q]; }, [&](int q) { return dl[q]; },
+          [&](int q) { return q0 + q < n && (!CAUSAL || key <= q0 + q); }, any_masked);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full));
+    }
+    if (ok) {
+      ok = wait_phase(smem_u32(&ctl->o_full), 0, abort_flag, status);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const bool live = key < n;
+      const size_t row_off = (static_cast<size_t>(bh) * n + (live ? key : 0)) * D + G::kHalfCols * hc;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {   // 0: dV (cols 256..), 1: dK (cols 384..)
+        const uint32_t t_acc = tmem + lane_addr + (which ? 384 : 256) + G::kHalfCols * hc;
+        const float mult = which ? args.scale : 1.f;
+        __nv_bfloat16* dst = (which ? args.g0 : args.g1) + row_off;
+#pragma unroll
+        for (int cb = 0; cb < G::kHalfCols / 32; ++cb) {
+          uint32_t rr[32];
+          tmem_ld32(t_acc + cb * 32, rr);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * mult,
+                                __uint_as_float(rr[2 * i + 1]) * mult);
+          if (live) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + cb * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// dQ: one CTA per (head, query block).  Grid (query blocks, BH); causal: (BH, query blocks) with
+// the query blocks in decreasing order (the heaviest first).
+// ------------------------------------------------------------------------------------------
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                  const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
+                  const BwdArgs args) {
+  using G = BwdGeo<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* s_q = smem;
+  uint8_t* s_do = smem + G::kTileBytes;
+  uint8_t* s_ring = smem + 2 * G::kTileBytes;  // stage s: K at 2s, V at 2s + 1 (tiles)
+  BwdCtrl* ctl = reinterpret_cast<BwdCtrl*>(smem + 6 * G::kTileBytes);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int n = args.n;
+  const int nblk = (n + kTileRows - 1) / kTileRows;
+  const int bh = CAUSAL ? blockIdx.x : blockIdx.y;
+  const int iblk = CAUSAL ? (nblk - 1 - static_cast<int>(blockIdx.y)) : blockIdx.x;
+  const int nk = CAUSAL ? iblk + 1 : nblk;   // key blocks visited
+  int* const status = args.status;
+
+  if (warp == 9) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), 512);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&ctl->fix_full), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&ctl->ring_full[s]), 1);
+      mbar_init(smem_u32(&ctl->ring_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&ctl->s_full), 1);
+    mbar_init(smem_u32(&ctl->p_full), 8);
+    mbar_init(smem_u32(&ctl->o_full), 1);
+    mbar_init(smem_u32(&ctl->drain), 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  int* abort_flag = &ctl->abort;
+
+  if (warp >= 8) {
+    regs_dec<72>();
+    if (warp == 8) {
+      if (lane == 0) {
+        tma_prefetch_map(&map_q);
+        tma_prefetch_map(&map_k);
+        tma_prefetch_map(&map_v);
+        tma_prefetch_map(&map_do);
+        const uint32_t fb = smem_u32(&ctl->fix_full);
+        mbar_arrive_expect_tx(fb, 2 * G::kTileBytes);
+        for (int b = 0; b < G::kBoxes; ++b) {
+          tma_load_3d(smem_u32(s_q + b * kTileRows * 128), &map_q, fb, b * 64, iblk * kTileRows, bh);
+          tma_load_3d(smem_u32(s_do + b * kTileRows * 128), &map_do, fb, b * 64, iblk * kTileRows, bh);
+        }
+        bool ok = true;
+        int issued = 0;
+        for (int u = 0; u < nk && ok; ++u) {
+          const int s = u & 1;
+          if (u >= 2) {
+            ok = wait_phase(smem_u32(&ctl->ring_empty[s]), ((u >> 1) - 1) & 1, abort_flag, status);
+            if (!ok) break;
+          }
+          const uint32_t rb = smem_u32(&ctl->ring_full[s]);
+          mbar_arrive_expect_tx(rb, 2 * G::kTileBytes);
+          uint8_t* dk = s_ring + (2 * s) * G::kTileBytes;
+          uint8_t* dv = s_ring + (2 * s + 1) * G::kTileBytes;
+          for (int b = 0; b < G::kBoxes; ++b) {
+            tma_load_3d(smem_u32(dk + b * kTileRows * 128), &map_k, rb, b * 64, u * kTileRows, bh);
+            tma_load_3d(smem_u32(dv + b * kTileRows * 128), &map_v, rb, b * 64, u * kTileRows, bh);
+          }
+          ++issued;
+        }
+        if (!ok) {
+          wait_phase(fb, 0, abort_flag, status);
+          for (int u = issued > 2 ? issued - 2 : 0; u < issued; ++u) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(smem_u32(&ctl->ring_full[u & 1]), (u >> 1) & 1) &&
+                   globaltimer_ns() - t0 < kWaitLimitNs) {
+            }
+          }
+        }
+      }
+    } else if (warp == 9) {
+      if (lane == 0) {
+        bool ok = wait_phase(smem_u32(&ctl->fix_full), 0, abort_flag, status);
+        tc_fence_after();
+        const uint32_t q_tile = smem_u32(s_q), do_tile = smem_u32(s_do);
+        for (int u = 0; u < nk && ok; ++u) {
+          const int s = u & 1;
+          ok = wait_phase(smem_u32(&ctl->ring_full[s]), (u >> 1) & 1, abort_flag, status);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t k_tile = smem_u32(s_ring + (2 * s) * G::kTileBytes);
+          const uint32_t v_tile = smem_u32(s_ring + (2 * s + 1) * G::kTileBytes);
+          mma_s_type<D>(tmem, q_tile, k_tile);           // S  = Q_i K_j^T
+          mma_s_type<D>(tmem + 128, do_tile, v_tile);    // dP = dO_i V_j^T
+          tc_commit(smem_u32(&ctl->s_full));
+          ok = wait_phase(smem_u32(&ctl->p_full), u & 1, abort_flag, status);
+          if (!ok) break;
+          tc_fence_after();
+          mma_acc<D>(tmem + 256, tmem + 128, k_tile, u > 0);   // dQ += dS K_j
+          tc_commit(smem_u32(&ctl->ring_empty[s]));
+        }
+        if (ok) tc_commit(smem_u32(&ctl->o_full));
+        tc_commit(smem_u32(&ctl->drain));
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(smem_u32(&ctl->drain), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+  } else {
+    regs_inc<216>();
+    const int w4 = warp % 4, hc = warp / 4;
+    const int r = w4 * 32 + lane;                  // query row within the block (TMEM lane)
+    const int row = iblk * kTileRows + r;
+    const bool live = row < n;
+    const size_t ridx = static_cast<size_t>(bh) * n + (live ? row : 0);
+    const float lse2_row = live ? args.lse[ridx] * kLog2e : 0.f;
+    const float d_row = live ? args.delta[ridx] : 0.f;
+    const uint32_t lane_addr = static_cast<uint32_t>(w4 * 32) << 16;
+    const uint32_t t_s = tmem + lane_addr + 64 * hc;
+    const uint32_t t_dp = tmem + lane_addr + 128 + 64 * hc;
+    bool ok = true;
+    for (int u = 0; u < nk && ok; ++u) {
+      ok = wait_phase(smem_u32(&ctl->s_full), u & 1, abort_flag, status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const int k0 = u * kTileRows + 64 * hc;      // first key column of this half
+      const bool any_masked = (CAUSAL && u == iblk) || (u + 1) * kTileRows > n;
+      // dS lands over the dP columns (tmem + 128), where the dQ product takes its A operand
+      softmax_half(
+          t_s, t_dp, args.c, [&](int) { return lse2_row; }, [&](int) { return d_row; },
+          [&](int k) { return k0 + k < n && (!CAUSAL || k0 + k <= row); }, any_masked);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full));
+    }
+    if (ok) {
+      ok = wait_phase(smem_u32(&ctl->o_full), 0, abort_flag, status);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const uint32_t t_acc = tmem + lane_addr + 256 + G::kHalfCols * hc;
+      __nv_bfloat16* dst = args.g0 + ridx * D + G::kHalfCols * hc;
+#pragma unroll
+      for (int cb = 0; cb < G::kHalfCols / 32; ++cb) {
+        uint32_t rr[32];
+        tmem_ld32(t_acc + cb * 32, rr);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * args.scale,
+                              __uint_as_float(rr[2 * i + 1]) * args.scale);
+        if (live) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + cb * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace exattn

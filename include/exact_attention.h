@@ -202,6 +202,29 @@ FA_API int fa_quantize_e4m3(const void* x, void* codes, float* descales, int B, 
                             int d, const float* signs, int flags, void* stream);
 
 /*
+ * Attention backward for bf16 operands ("FlashAttention · InkStack", section 1.2: dV = P^T dO,
+ * dP = dO V^T, dS = P * (dP - D) with D_i = rowsum(dO_i * O_i), dQ = scale dS K,
+ * dK = scale dS^T Q; P recomputed from the forward's LSE as in section 1.2.2).  Three kernel
+ * launches on `stream`: D, then dK/dV, then dQ.
+ *   q, k, v, o, dout : device pointers, [B, H, N, d] bf16 (16-byte aligned); o and lse are the
+ *                      forward outputs for q, k, v (same scale and mask)
+ *   lse              : device pointer, [B, H, N] fp32 (4-byte aligned), natural log
+ *   dq, dk, dv       : device pointers, [B, H, N, d] bf16 outputs (16-byte aligned)
+ *   workspace        : caller-owned device scratch of fa_bwd_workspace_bytes(B, H, N) bytes
+ *                      (16-byte aligned), holds D; contents on entry do not matter
+ *   dev_status       : as fa_fwd_opts.dev_status (NULL = the library's status word)
+ * Sizes, scale, mask and errors as fa_fwd (d in {64, 128}); too small a workspace is
+ * FA_ERR_INVALID_ARG.
+ */
+FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                  float scale, int causal, void* workspace, size_t workspace_bytes,
+                  int* dev_status, void* stream);
+
+/* Workspace bytes fa_bwd needs: B * H * N * 4, rounded up to 256; 0 for invalid arguments. */
+FA_API size_t fa_bwd_workspace_bytes(int B, int H, int N);
+
+/*
  * Read, and if `clear` is nonzero reset to FA_OK, the library's status word on the current
  * device.  Synchronises the device first.  Writes FA_OK or FA_ERR_DEVICE_TIMEOUT to *out.
  * Returns an fa_status for the call itself.

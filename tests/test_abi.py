@@ -133,3 +133,25 @@ def test_quantize_host_checks(lib, args, want):
 def test_quantize_rejects_unknown_flags(lib):
     assert ea.fa_quantize_e4m3(FAKE, FAKE, FAKE, 1, 1, 128, 128, None, 2, None) == \
         ea.FA_ERR_INVALID_ARG
+
+
+def test_bwd_workspace_bytes(lib):
+    assert ea.bwd_workspace_bytes(1, 2, 300) == (2 * 300 * 4 + 255) // 256 * 256
+    assert ea.bwd_workspace_bytes(0, 1, 8) == 0
+
+
+@pytest.mark.parametrize("patch,want", [
+    ({0: 0}, ea.FA_ERR_INVALID_ARG),            # null q
+    ({15: 0}, ea.FA_ERR_INVALID_ARG),           # null workspace
+    ({16: 16}, ea.FA_ERR_INVALID_ARG),          # workspace too small
+    ({12: 96}, ea.FA_ERR_UNSUPPORTED),          # d = 96
+    ({13: -1.0}, ea.FA_ERR_INVALID_ARG),        # negative scale
+    ({6: FAKE + 8}, ea.FA_ERR_MISALIGNED),      # dq misaligned
+    ({4: FAKE + 2}, ea.FA_ERR_MISALIGNED),      # lse misaligned
+])
+def test_bwd_host_checks(lib, patch, want):
+    args = [FAKE] * 9 + [1, 1, 128, 128, 0.1, 0, FAKE, ea.bwd_workspace_bytes(1, 1, 128), None,
+                         None]
+    for i, val in patch.items():
+        args[i] = val
+    assert ea.fa_bwd(*args) == want
