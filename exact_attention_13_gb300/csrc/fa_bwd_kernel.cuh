@@ -61,14 +61,16 @@ struct BwdCtrl {
   uint64_t ring_full[2];  // streamed pair (dK/dV: Q_i, dO_i; dQ: K_j, V_j)
   uint64_t ring_empty[2];
   uint64_t vec_full[2];   // LSE and D of the query block (dK/dV)
-  uint64_t s_full;        // both S-type products of the step are in TMEM
-  uint64_t p_full;        // P / dS written back (eight warps)
+  uint64_t s_full;        // S (dK/dV: S^T) of the step is in TMEM
+  uint64_t dp_full;       // dP (dP^T) of the step is in TMEM
+  uint64_t p_full;        // P^T written back in bf16 (eight warps; dK/dV)
+  uint64_t ds_full;       // dS (dS^T) written back in bf16 (eight warps)
   uint64_t o_full;        // the last accumulating product is done
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-  float lse2[2][kTileRows];   // LSE * log2(e) of the stage's 128 queries
-  float dlt[2][kTileRows];    // D of the stage's 128 queries
+  alignas(16) float lse2[2][kTileRows];   // LSE * log2(e) of the stage's 128 queries
+  alignas(16) float dlt[2][kTileRows];    // D of the stage's 128 queries
 };
 
 // two fixed tiles + two ring stages of two tiles + the control block
@@ -130,45 +132,85 @@ __device__ __forceinline__ void mma_acc(uint32_t tmem_d, uint32_t tmem_a, uint32
                G::kIdescAcc, (accumulate || kb > 0) ? 1u : 0u);
 }
 
-// Half-row softmax step shared by both kernels: 64 scores s and 64 dP values of this thread's
-// row, turned into P (bf16, written over the S columns) and dS = P (dP - D) (bf16, over the dP
-// columns).  lse2/dlt give each column's LSE * log2(e) and D (dK/dV kernel: per query column;
-// dQ kernel: the row's own values repeated); `visible` says which columns are unmasked.
-template <typename LseFn, typename DltFn, typename VisFn>
-__device__ __forceinline__ void softmax_half(uint32_t t_s, uint32_t t_dp, float c, LseFn lse2,
-                                             DltFn dlt, VisFn visible, bool any_masked) {
-  float s[64], dp[64];
-  {
-    uint32_t r0[32], r1[32], r2[32], r3[32];
-    tmem_ld32(t_s, r0);
-    tmem_ld32(t_s + 32, r1);
-    tmem_ld32(t_dp, r2);
-    tmem_ld32(t_dp + 32, r3);
+// Half-row softmax steps shared by both kernels, for the 64 columns of this thread's row.
+// softmax_p: P = 2^(s c - LSE log2 e) from the S columns into p[] (fp32), and, when STORE, as
+// bf16 over the S columns (dK/dV kernel: the A operand of dV += P^T dO).  softmax_ds:
+// dS = P (dP - D) from the dP columns, as bf16 over them.  Both run in two passes of 32 columns;
+// the bf16 results of pass 0 land in columns 0-15 and of pass 1 in columns 16-31 of the thread's
+// range, whose fp32 values were read in pass 0.  PER_COLUMN (dK/dV kernel): column q has its own
+// LSE * log2(e) and D, read as float4 from the shared arrays; otherwise (dQ kernel) the row's
+// own values apply to every column.  `visible` masks columns when any_masked.
+template <bool PER_COLUMN, bool STORE, typename VisFn>
+__device__ __forceinline__ void softmax_p(uint32_t t_s, float c, const float* l2, float l2_row,
+                                          VisFn visible, bool any_masked, float (&p)[64]) {
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    uint32_t rs[32];
+    tmem_ld32(t_s + 32 * pass, rs);
+    float lv[32];
+    if constexpr (PER_COLUMN) {
+      const float4* l4 = reinterpret_cast<const float4*>(l2 + 32 * pass);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 a = l4[i];
+        lv[4 * i] = a.x;
+        lv[4 * i + 1] = a.y;
+        lv[4 * i + 2] = a.z;
+        lv[4 * i + 3] = a.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) lv[i] = l2_row;
+    }
     tmem_ld_wait();
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      s[i] = __uint_as_float(r0[i]);
-      s[32 + i] = __uint_as_float(r1[i]);
-      dp[i] = __uint_as_float(r2[i]);
-      dp[32 + i] = __uint_as_float(r3[i]);
+      float x = ex2_mufu(fmaf(__uint_as_float(rs[i]), c, -lv[i]));
+      if (any_masked) x = visible(32 * pass + i) ? x : 0.f;
+      p[32 * pass + i] = x;
     }
-  }
-  uint32_t pp[32], pd[32];
+    if constexpr (STORE) {
+      uint32_t pp[16];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    float p0 = ex2_mufu(fmaf(s[2 * i], c, -lse2(2 * i)));
-    float p1 = ex2_mufu(fmaf(s[2 * i + 1], c, -lse2(2 * i + 1)));
-    if (any_masked) {
-      p0 = visible(2 * i) ? p0 : 0.f;
-      p1 = visible(2 * i + 1) ? p1 : 0.f;
+      for (int i = 0; i < 16; ++i) pp[i] = pack_bf16x2(p[32 * pass + 2 * i], p[32 * pass + 2 * i + 1]);
+      tmem_st16(t_s + 16 * pass, pp);
     }
-    const float d0 = p0 * (dp[2 * i] - dlt(2 * i));
-    const float d1 = p1 * (dp[2 * i + 1] - dlt(2 * i + 1));
-    pp[i] = pack_bf16x2(p0, p1);
-    pd[i] = pack_bf16x2(d0, d1);
   }
-  tmem_st32(t_s, pp);
-  tmem_st32(t_dp, pd);
+  if constexpr (STORE) tmem_st_wait();
+}
+
+template <bool PER_COLUMN>
+__device__ __forceinline__ void softmax_ds(uint32_t t_dp, const float* dl, float dl_row,
+                                           const float (&p)[64]) {
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    uint32_t rd[32];
+    tmem_ld32(t_dp + 32 * pass, rd);
+    float dv[32];
+    if constexpr (PER_COLUMN) {
+      const float4* d4 = reinterpret_cast<const float4*>(dl + 32 * pass);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 b = d4[i];
+        dv[4 * i] = b.x;
+        dv[4 * i + 1] = b.y;
+        dv[4 * i + 2] = b.z;
+        dv[4 * i + 3] = b.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) dv[i] = dl_row;
+    }
+    tmem_ld_wait();
+    uint32_t pd[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int q = 32 * pass + 2 * i;
+      pd[i] = pack_bf16x2(p[q] * (__uint_as_float(rd[2 * i]) - dv[2 * i]),
+                          p[q + 1] * (__uint_as_float(rd[2 * i + 1]) - dv[2 * i + 1]));
+    }
+    tmem_st16(t_dp + 16 * pass, pd);
+  }
   tmem_st_wait();
 }
 
@@ -212,7 +254,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(smem_u32(&ctl->vec_full[s]), 1);
     }
     mbar_init(smem_u32(&ctl->s_full), 1);
+    mbar_init(smem_u32(&ctl->dp_full), 1);
     mbar_init(smem_u32(&ctl->p_full), 8);
+    mbar_init(smem_u32(&ctl->ds_full), 8);
     mbar_init(smem_u32(&ctl->o_full), 1);
     mbar_init(smem_u32(&ctl->drain), 1);
     ctl->abort = 0;
@@ -282,13 +326,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_after();
           const uint32_t q_tile = smem_u32(s_ring + (2 * s) * G::kTileBytes);
           const uint32_t do_tile = smem_u32(s_ring + (2 * s + 1) * G::kTileBytes);
+          // the softmax turns S^T into P^T while the tensor core computes dP^T, and dP^T into
+          // dS^T while it accumulates dV
           mma_s_type<D>(tmem, k_tile, q_tile);          // S^T  = K_j Q_i^T
-          mma_s_type<D>(tmem + 128, v_tile, do_tile);   // dP^T = V_j dO_i^T
           tc_commit(smem_u32(&ctl->s_full));
+          mma_s_type<D>(tmem + 128, v_tile, do_tile);   // dP^T = V_j dO_i^T
+          tc_commit(smem_u32(&ctl->dp_full));
           ok = wait_phase(smem_u32(&ctl->p_full), u & 1, abort_flag, status);
           if (!ok) break;
           tc_fence_after();
           mma_acc<D>(tmem + 256, tmem, do_tile, u > 0);        // dV += P^T dO_i
+          ok = wait_phase(smem_u32(&ctl->ds_full), u & 1, abort_flag, status);
+          if (!ok) break;
+          tc_fence_after();
           mma_acc<D>(tmem + 384, tmem + 128, q_tile, u > 0);   // dK += dS^T Q_i
           tc_commit(smem_u32(&ctl->ring_empty[s]));
         }
@@ -341,12 +391,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float* dl = ctl->dlt[s] + 64 * hc;
       const int q0 = qblk * kTileRows + 64 * hc;   // first query column of this half
       const bool any_masked = (CAUSAL && qblk == jblk) || (qblk + 1) * kTileRows > n;
-      softmax_half(
-          t_s, t_dp, args.c, [&](int q) { return l2[q]; }, [&](int q) { return dl[q]; },
-          [&](int q) { return q0 + q < n && (!CAUSAL || key <= q0 + q); }, any_masked);
+      float p[64];
+      softmax_p<true, true>(t_s, args.c, l2, 0.f,
+                            [&](int q) { return q0 + q < n && (!CAUSAL || key <= q0 + q); },
+                            any_masked, p);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full));
+      ok = wait_phase(smem_u32(&ctl->dp_full), u & 1, abort_flag, status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      softmax_ds<true>(t_dp, dl, 0.f, p);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->ds_full));
     }
     if (ok) {
       ok = wait_phase(smem_u32(&ctl->o_full), 0, abort_flag, status);
@@ -428,7 +487,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(smem_u32(&ctl->ring_empty[s]), 1);
     }
     mbar_init(smem_u32(&ctl->s_full), 1);
+    mbar_init(smem_u32(&ctl->dp_full), 1);
     mbar_init(smem_u32(&ctl->p_full), 8);
+    mbar_init(smem_u32(&ctl->ds_full), 8);
     mbar_init(smem_u32(&ctl->o_full), 1);
     mbar_init(smem_u32(&ctl->drain), 1);
     ctl->abort = 0;
@@ -495,9 +556,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const uint32_t k_tile = smem_u32(s_ring + (2 * s) * G::kTileBytes);
           const uint32_t v_tile = smem_u32(s_ring + (2 * s + 1) * G::kTileBytes);
           mma_s_type<D>(tmem, q_tile, k_tile);           // S  = Q_i K_j^T
-          mma_s_type<D>(tmem + 128, do_tile, v_tile);    // dP = dO_i V_j^T
           tc_commit(smem_u32(&ctl->s_full));
-          ok = wait_phase(smem_u32(&ctl->p_full), u & 1, abort_flag, status);
+          mma_s_type<D>(tmem + 128, do_tile, v_tile);    // dP = dO_i V_j^T
+          tc_commit(smem_u32(&ctl->dp_full));
+          ok = wait_phase(smem_u32(&ctl->ds_full), u & 1, abort_flag, status);
           if (!ok) break;
           tc_fence_after();
           mma_acc<D>(tmem + 256, tmem + 128, k_tile, u > 0);   // dQ += dS K_j
@@ -530,13 +592,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       const int k0 = u * kTileRows + 64 * hc;      // first key column of this half
       const bool any_masked = (CAUSAL && u == iblk) || (u + 1) * kTileRows > n;
+      float p[64];
+      softmax_p<false, false>(t_s, args.c, nullptr, lse2_row,
+                              [&](int k) { return k0 + k < n && (!CAUSAL || k0 + k <= row); },
+                              any_masked, p);
+      ok = wait_phase(smem_u32(&ctl->dp_full), u & 1, abort_flag, status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
       // dS lands over the dP columns (tmem + 128), where the dQ product takes its A operand
-      softmax_half(
-          t_s, t_dp, args.c, [&](int) { return lse2_row; }, [&](int) { return d_row; },
-          [&](int k) { return k0 + k < n && (!CAUSAL || k0 + k <= row); }, any_masked);
+      softmax_ds<false>(t_dp, nullptr, d_row, p);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full));
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->ds_full));
     }
     if (ok) {
       ok = wait_phase(smem_u32(&ctl->o_full), 0, abort_flag, status);
