@@ -248,6 +248,19 @@ def run_ours(args, w, world, rank, local):
     inp = make_inputs(w)
     q, k, v = (getattr(inp, n).to(dev) for n in "qkv")
     descale = (inp.descale_q, inp.descale_k, inp.descale_v)
+    # fp8 with block descales: the operands are the bf16 draws quantised on the GPU, one descale
+    # per 128-row block (power-of-two descales for V)
+    block = w.dtype == "e4m3" and args.fp8_scaling == "block"
+    scales = ()
+    if block:
+        from workloads import random_inputs
+
+        src = random_inputs(w.B, w.H, w.N, w.d, "bf16", w.seed)
+        q, dq_b = ea.quantize_e4m3(src.q.to(dev))
+        k, dk_b = ea.quantize_e4m3(src.k.to(dev))
+        v, dv_b = ea.quantize_e4m3(src.v.to(dev), pow2=True)
+        scales = (dq_b, dk_b, dv_b)
+        del src
     o = torch.empty(w.B, w.H, w.N, w.d, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -260,9 +273,16 @@ def run_ours(args, w, world, rank, local):
 
     pv16 = args.fp8_pv == "f16"
 
+    def attn(q_, k_, v_, o_, l_, sc_):
+        if block:
+            ea.fwd_fp8_blockscaled(q_, k_, v_, *sc_, causal=w.causal, scale=w.scale, out=o_,
+                                   lse=l_, num_splits=splits, workspace=workspace, pv16=pv16)
+        else:
+            ea.fwd(q_, k_, v_, causal=w.causal, scale=w.scale, descale=descale, out=o_, lse=l_,
+                   num_splits=splits, workspace=workspace, pv16=pv16)
+
     def step():
-        ea.fwd(q, k, v, causal=w.causal, scale=w.scale, descale=descale, out=o, lse=lse,
-               num_splits=splits, workspace=workspace, pv16=pv16)
+        attn(q, k, v, o, lse, scales)
 
     for _ in range(args.warmup):
         step()
@@ -294,7 +314,9 @@ def run_ours(args, w, world, rank, local):
     # Pipelined the way a serving loop runs it: two device buffer sets, H2D on one stream, the
     # kernel on another, D2H on a third; step i's copies overlap steps i-1 / i+1's kernels, and
     # every step still moves its own inputs in and its own outputs out.
-    qh, kh, vh = (getattr(inp, n).pin_memory() for n in "qkv")
+    qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+    sh = [t.cpu().pin_memory() for t in scales]
+    dsc = [list(scales), [torch.empty_like(t) for t in scales]]
     oh = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for _ in range(2)]
     lh = [torch.empty(lse.shape, dtype=lse.dtype).pin_memory() for _ in range(2)]
     dq = [q, torch.empty_like(q)]
@@ -315,12 +337,13 @@ def run_ours(args, w, world, rank, local):
             dq[b].copy_(qh, non_blocking=True)
             dk[b].copy_(kh, non_blocking=True)
             dv[b].copy_(vh, non_blocking=True)
+            for dst, srcp in zip(dsc[b], sh):
+                dst.copy_(srcp, non_blocking=True)
         ev["in"][b].record(s_in)
         s_cmp.wait_event(ev["in"][b])
         s_cmp.wait_event(ev["out"][b])         # the D2H that last read outputs b is done
         with torch.cuda.stream(s_cmp):
-            ea.fwd(dq[b], dk[b], dv[b], causal=w.causal, scale=w.scale, descale=descale,
-                   out=do[b], lse=dl[b], num_splits=splits, workspace=workspace, pv16=pv16)
+            attn(dq[b], dk[b], dv[b], do[b], dl[b], dsc[b])
         ev["cmp"][b].record(s_cmp)
         s_out.wait_event(ev["cmp"][b])
         with torch.cuda.stream(s_out):
@@ -342,7 +365,7 @@ def run_ours(args, w, world, rank, local):
     torch.cuda.synchronize()
     e_ms = max_over_ranks(e_start.elapsed_time(e_end) / args.steps, world, dev)
     assert ea.device_status() == 0, "device wait timed out during the end-to-end run"
-    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh, *sh))
     d2h = oh[0].numel() * oh[0].element_size() + lh[0].numel() * lh[0].element_size()
 
     flops_rank = w.flops
@@ -363,8 +386,10 @@ def run_ours(args, w, world, rank, local):
         peak_note = " x 2 (nominal fp8:bf16)" if is_fp8 else ""
     achieved = flops_rank / (ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": measured_traffic(w.name, args.traffic_bytes,
-                                                      "pv16" if is_fp8 and pv16 else ""),
+                "frac": achieved / peak,
+                "traffic": measured_traffic(w.name, args.traffic_bytes, "_".join(
+                    ([("pv16" if pv16 else "")] if is_fp8 else []) + (["block"] if block else []))
+                    .strip("_")),
                 "peak_kind": f"{pk['source']} cuBLAS bf16 burst" + peak_note,
                 "kernel": "exattn::fa_fwd_kernel"}
     # exp-unit bound at the clock seen during the run (informative)
@@ -381,7 +406,8 @@ def run_ours(args, w, world, rank, local):
                    "heads": w.H, "seq_len": w.N, "head_dim": w.d, "causal": w.causal,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "key_splits": args.splits,
-                   **({"pv_product": args.fp8_pv} if is_fp8 else {}),
+                   **({"pv_product": args.fp8_pv, "fp8_scaling": args.fp8_scaling}
+                      if is_fp8 else {}),
                    "l2": "inputs larger than L2 (no flush)" if 3 * q.numel() * q.element_size()
                    > 129e6 else "inputs smaller than L2"},
         "pct_of_peak": 100.0 * achieved / peak,
@@ -538,6 +564,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fp8-pv", default="e4m3", choices=["e4m3", "f16"],
                     help="fp8 operands: precision of the P V product")
+    ap.add_argument("--fp8-scaling", default="tensor", choices=["tensor", "block"],
+                    help="fp8 operands: one descale per tensor, or per 128-row block")
     ap.add_argument("--op", default="attention", choices=["attention", "quantize", "backward"],
                     help="attention forward (default), the fp8 block quantiser alone, or the "
                          "attention backward")

@@ -200,6 +200,14 @@ def test_fp8_accuracy_study(ea):
     qh, dqh = ea.quantize_e4m3(q, signs=signs)
     kh, dkh = ea.quantize_e4m3(k, signs=signs)
     res["fp8_block_hadamard"] = rmse(ea.fwd_fp8_blockscaled(qh, kh, vb, dqh, dkh, dv)[0])
+    # ablation: the transform with one descale per tensor ("no block quantisation"); the
+    # transformed operands are formed here with a dense fp32 product by diag(s) H / sqrt(d)
+    m = torch.from_numpy(qz.incoherent_transform(np.eye(d), hadamard_signs(d, 77).numpy()))
+    m = m.to(torch.float32)
+    qt, kt = (getattr(inp, n).float() @ m for n in "qk")
+    ptq = [quantize_e4m3(t) for t in (qt, kt, inp.v.float())]
+    res["fp8_per_tensor_hadamard"] = rmse(ea.fwd(*(c.to(DEV) for c, _ in ptq),
+                                                 descale=tuple(s_ for _, s_ in ptq))[0])
     # the same three fp8 variants with an f16 P V product
     res["fp8_per_tensor_pv16"] = rmse(ea.fwd(*(c.to(DEV) for c, _ in pt),
                                              descale=tuple(s for _, s in pt), pv16=True)[0])
@@ -211,4 +219,5 @@ def test_fp8_accuracy_study(ea):
     assert res["bf16"] < 1e-3
     assert res["fp8_block_hadamard"] < res["fp8_per_tensor"]
     assert res["fp8_block_hadamard"] < res["fp8_block"]
+    assert res["fp8_per_tensor_hadamard"] < res["fp8_per_tensor"]
     assert max(res.values()) < 5e-2
