@@ -250,21 +250,30 @@ template <bool MASKED, PFmt PF, int P_PARTS, int EMU_EVERY>
 __device__ __forceinline__ float exp_and_publish(float (&s)[128], float c, float m, int lim,
                                                  uint32_t t_s, uint32_t bar0, uint32_t bar1,
                                                  int lane) {
-  float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  // eight partial sums (element i goes to sum i % 8), kept as four packed pairs; the exponent
+  // arguments s c - m are formed two at a time (same rounding as the scalar fma)
+  uint64_t ps2[4] = {0ull, 0ull, 0ull, 0ull};
+  const uint64_t c2 = f32x2(c, c), nm2 = f32x2(-m, -m);
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
 #pragma unroll
-    for (int i = 64 * half; i < 64 * half + 64; ++i) {
-      const float x = fmaf(s[i], c, -m);
-      float p;
-      if constexpr (MASKED)
-        p = i < lim ? ex2_mufu(x) : 0.f;
-      else if constexpr (EMU_EVERY > 0)
-        p = (i % EMU_EVERY == EMU_EVERY - 1) ? ex2_poly(x) : ex2_mufu(x);
-      else
-        p = ex2_mufu(x);
-      s[i] = p;
-      ps[i % 8] += p;
+    for (int i = 64 * half; i < 64 * half + 64; i += 2) {
+      const uint64_t x2 = fma_f32x2(f32x2(s[i], s[i + 1]), c2, nm2);
+      const float x0 = f32x2_lo(x2), x1 = f32x2_hi(x2);
+      float p0, p1;
+      if constexpr (MASKED) {
+        p0 = i < lim ? ex2_mufu(x0) : 0.f;
+        p1 = i + 1 < lim ? ex2_mufu(x1) : 0.f;
+      } else if constexpr (EMU_EVERY > 0) {
+        p0 = (i % EMU_EVERY == EMU_EVERY - 1) ? ex2_poly(x0) : ex2_mufu(x0);
+        p1 = ((i + 1) % EMU_EVERY == EMU_EVERY - 1) ? ex2_poly(x1) : ex2_mufu(x1);
+      } else {
+        p0 = ex2_mufu(x0);
+        p1 = ex2_mufu(x1);
+      }
+      s[i] = p0;
+      s[i + 1] = p1;
+      ps2[(i / 2) % 4] = add_f32x2(ps2[(i / 2) % 4], f32x2(p0, p1));
     }
     if constexpr (PF == PFmt::kE4m3) {
       uint32_t r[16];
@@ -288,6 +297,12 @@ __device__ __forceinline__ float exp_and_publish(float (&s)[128], float c, float
       __syncwarp();
       if (lane == 0) mbar_arrive(half == 0 ? bar0 : bar1);
     }
+  }
+  float ps[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    ps[2 * k] = f32x2_lo(ps2[k]);
+    ps[2 * k + 1] = f32x2_hi(ps2[k]);
   }
 #pragma unroll
   for (int w = 4; w >= 1; w /= 2)
@@ -671,12 +686,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 128; ++i)
           if (i >= lim) s[i] = -INFINITY;
       }
-      // row max: eight independent partial maxima, then a tree
+      // row max: eight independent partial maxima folding two columns per instruction, then a
+      // tree
       float mp[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mp[k] = s[k];
+      for (int k = 0; k < 8; ++k) mp[k] = fmaxf(s[2 * k], s[2 * k + 1]);
 #pragma unroll
-      for (int i = 8; i < 128; ++i) mp[i % 8] = fmaxf(mp[i % 8], s[i]);
+      for (int i = 16; i < 128; i += 2) mp[(i / 2) % 8] = max3f(mp[(i / 2) % 8], s[i], s[i + 1]);
 #pragma unroll
       for (int w = 4; w >= 1; w /= 2)
 #pragma unroll
@@ -696,8 +712,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cb = 0; cb < D / 32; ++cb) {
           tmem_ld32(t_o + cb * 32, r);
           tmem_ld_wait();
+          const uint64_t a2 = f32x2(alpha, alpha);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          for (int i = 0; i < 32; i += 2) {
+            const uint64_t v = mul_f32x2(f32x2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), a2);
+            r[i] = __float_as_uint(f32x2_lo(v));
+            r[i + 1] = __float_as_uint(f32x2_hi(v));
+          }
           tmem_st32(t_o + cb * 32, r);
         }
         l_run *= alpha;
