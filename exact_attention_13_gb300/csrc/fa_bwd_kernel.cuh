@@ -163,11 +163,19 @@ __device__ __forceinline__ void softmax_p(uint32_t t_s, float c, const float* l2
       for (int i = 0; i < 32; ++i) lv[i] = l2_row;
     }
     tmem_ld_wait();
+    const uint64_t c2 = f32x2(c, c);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      float x = ex2_mufu(fmaf(__uint_as_float(rs[i]), c, -lv[i]));
-      if (any_masked) x = visible(32 * pass + i) ? x : 0.f;
-      p[32 * pass + i] = x;
+    for (int i = 0; i < 32; i += 2) {
+      // s c - LSE log2(e) for two columns in one packed fma
+      const uint64_t x2 = fma_f32x2(f32x2(__uint_as_float(rs[i]), __uint_as_float(rs[i + 1])), c2,
+                                    f32x2(-lv[i], -lv[i + 1]));
+      float x0 = ex2_mufu(f32x2_lo(x2)), x1 = ex2_mufu(f32x2_hi(x2));
+      if (any_masked) {
+        x0 = visible(32 * pass + i) ? x0 : 0.f;
+        x1 = visible(32 * pass + i + 1) ? x1 : 0.f;
+      }
+      p[32 * pass + i] = x0;
+      p[32 * pass + i + 1] = x1;
     }
     if constexpr (STORE) {
       uint32_t pp[16];
@@ -206,8 +214,11 @@ __device__ __forceinline__ void softmax_ds(uint32_t t_dp, const float* dl, float
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int q = 32 * pass + 2 * i;
-      pd[i] = pack_bf16x2(p[q] * (__uint_as_float(rd[2 * i]) - dv[2 * i]),
-                          p[q + 1] * (__uint_as_float(rd[2 * i + 1]) - dv[2 * i + 1]));
+      // dS = P (dP - D), two columns per packed add and multiply
+      const uint64_t t2 = add_f32x2(f32x2(__uint_as_float(rd[2 * i]), __uint_as_float(rd[2 * i + 1])),
+                                    f32x2(-dv[2 * i], -dv[2 * i + 1]));
+      const uint64_t d2 = mul_f32x2(f32x2(p[q], p[q + 1]), t2);
+      pd[i] = pack_bf16x2(f32x2_lo(d2), f32x2_hi(d2));
     }
     tmem_st16(t_dp + 16 * pass, pd);
   }
