@@ -63,7 +63,7 @@ struct BwdCtrl {
   uint64_t vec_full[2];   // LSE and D of the query block (dK/dV)
   uint64_t s_full;        // S (dK/dV: S^T) of the step is in TMEM
   uint64_t dp_full;       // dP (dP^T) of the step is in TMEM
-  uint64_t p_full;        // P^T written back in bf16 (eight warps; dK/dV)
+  uint64_t p_full;        // dK/dV: P^T written back in bf16; dQ: S read (eight warps)
   uint64_t ds_full;       // dS (dS^T) written back in bf16 (eight warps)
   uint64_t o_full;        // the last accumulating product is done
   uint64_t drain;
@@ -330,28 +330,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bool ok = wait_phase(smem_u32(&ctl->fix_full), 0, abort_flag, status);
         tc_fence_after();
         const uint32_t k_tile = smem_u32(s_k), v_tile = smem_u32(s_v);
-        for (int u = 0; u < nq && ok; ++u) {
-          const int s = u & 1;
-          ok = wait_phase(smem_u32(&ctl->ring_full[s]), (u >> 1) & 1, abort_flag, status);
-          if (!ok) break;
+        // Issue order per step u: dV(u), S(u+1), dK(u), dP(u+1).  S(u+1) overwrites P^T(u)
+        // only after dV(u) has read it (the tensor core runs one thread's MMAs in order), and
+        // dP(u+1) overwrites dS^T(u) after dK(u); so the softmax forms P^T(u+1) while dK(u)
+        // and dP(u+1) run, and dS^T(u+1) while dV(u+1) and S(u+2) run.
+        auto tile = [&](int u, int which) {
+          return smem_u32(s_ring + (2 * (u & 1) + which) * G::kTileBytes);
+        };
+        ok = ok && wait_phase(smem_u32(&ctl->ring_full[0]), 0, abort_flag, status);
+        if (ok) {
           tc_fence_after();
-          const uint32_t q_tile = smem_u32(s_ring + (2 * s) * G::kTileBytes);
-          const uint32_t do_tile = smem_u32(s_ring + (2 * s + 1) * G::kTileBytes);
-          // the softmax turns S^T into P^T while the tensor core computes dP^T, and dP^T into
-          // dS^T while it accumulates dV
-          mma_s_type<D>(tmem, k_tile, q_tile);          // S^T  = K_j Q_i^T
+          mma_s_type<D>(tmem, k_tile, tile(0, 0));          // S^T  = K_j Q_i^T
           tc_commit(smem_u32(&ctl->s_full));
-          mma_s_type<D>(tmem + 128, v_tile, do_tile);   // dP^T = V_j dO_i^T
+          mma_s_type<D>(tmem + 128, v_tile, tile(0, 1));    // dP^T = V_j dO_i^T
           tc_commit(smem_u32(&ctl->dp_full));
+        }
+        for (int u = 0; u < nq && ok; ++u) {
+          const bool more = u + 1 < nq;
           ok = wait_phase(smem_u32(&ctl->p_full), u & 1, abort_flag, status);
           if (!ok) break;
           tc_fence_after();
-          mma_acc<D>(tmem + 256, tmem, do_tile, u > 0);        // dV += P^T dO_i
+          mma_acc<D>(tmem + 256, tmem, tile(u, 1), u > 0);         // dV += P^T dO_i
+          if (more) {
+            ok = wait_phase(smem_u32(&ctl->ring_full[(u + 1) & 1]), ((u + 1) >> 1) & 1, abort_flag,
+                            status);
+            if (!ok) break;
+            tc_fence_after();
+            mma_s_type<D>(tmem, k_tile, tile(u + 1, 0));
+            tc_commit(smem_u32(&ctl->s_full));
+          }
           ok = wait_phase(smem_u32(&ctl->ds_full), u & 1, abort_flag, status);
           if (!ok) break;
           tc_fence_after();
-          mma_acc<D>(tmem + 384, tmem + 128, q_tile, u > 0);   // dK += dS^T Q_i
-          tc_commit(smem_u32(&ctl->ring_empty[s]));
+          mma_acc<D>(tmem + 384, tmem + 128, tile(u, 0), u > 0);   // dK += dS^T Q_i
+          tc_commit(smem_u32(&ctl->ring_empty[u & 1]));
+          if (more) {
+            mma_s_type<D>(tmem + 128, v_tile, tile(u + 1, 1));
+            tc_commit(smem_u32(&ctl->dp_full));
+          }
         }
         if (ok) tc_commit(smem_u32(&ctl->o_full));
         tc_commit(smem_u32(&ctl->drain));
@@ -361,6 +377,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     } else if (warp == 10) {
       // ------------------------------------------------------------ LSE / D stager
+      // The values of query block u + 1 are loaded into registers while block u's stage is
+      // being waited for and written, so the global-load latency is off the softmax's path.
+      constexpr int kPer = kTileRows / 32;
+      float lv[kPer], dv[kPer];
+      const float* lse_h = args.lse + static_cast<size_t>(bh) * n;
+      const float* dlt_h = args.delta + static_cast<size_t>(bh) * n;
+      auto fetch = [&](int u) {
+        const int row0 = (i0 + u) * kTileRows + lane;
+#pragma unroll
+        for (int t = 0; t < kPer; ++t) {
+          const int row = row0 + 32 * t;
+          lv[t] = row < n ? __ldg(lse_h + row) : 0.f;
+          dv[t] = row < n ? __ldg(dlt_h + row) : 0.f;
+        }
+      };
+      fetch(0);
       bool ok = true;
       for (int u = 0; u < nq && ok; ++u) {
         const int s = u & 1;
@@ -368,14 +400,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ok = wait_phase(smem_u32(&ctl->ring_empty[s]), ((u >> 1) - 1) & 1, abort_flag, status);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        const int row0 = (i0 + u) * kTileRows;
 #pragma unroll
-        for (int q = lane; q < kTileRows; q += 32) {
-          const int row = row0 + q;
-          const size_t idx = static_cast<size_t>(bh) * n + row;
-          ctl->lse2[s][q] = row < n ? args.lse[idx] * kLog2e : 0.f;
-          ctl->dlt[s][q] = row < n ? args.delta[idx] : 0.f;
+        for (int t = 0; t < kPer; ++t) {
+          ctl->lse2[s][lane + 32 * t] = lv[t] * kLog2e;
+          ctl->dlt[s][lane + 32 * t] = dv[t];
         }
+        if (u + 1 < nq) fetch(u + 1);
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&ctl->vec_full[s]));
       }
@@ -559,22 +589,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bool ok = wait_phase(smem_u32(&ctl->fix_full), 0, abort_flag, status);
         tc_fence_after();
         const uint32_t q_tile = smem_u32(s_q), do_tile = smem_u32(s_do);
-        for (int u = 0; u < nk && ok; ++u) {
-          const int s = u & 1;
-          ok = wait_phase(smem_u32(&ctl->ring_full[s]), (u >> 1) & 1, abort_flag, status);
-          if (!ok) break;
+        // Issue order per step u: S(u+1) once the softmax has read S(u), then dQ(u), dP(u+1);
+        // the tensor core computes S(u+1) while the softmax forms dS(u).
+        auto tile = [&](int u, int which) {
+          return smem_u32(s_ring + (2 * (u & 1) + which) * G::kTileBytes);
+        };
+        ok = ok && wait_phase(smem_u32(&ctl->ring_full[0]), 0, abort_flag, status);
+        if (ok) {
           tc_fence_after();
-          const uint32_t k_tile = smem_u32(s_ring + (2 * s) * G::kTileBytes);
-          const uint32_t v_tile = smem_u32(s_ring + (2 * s + 1) * G::kTileBytes);
-          mma_s_type<D>(tmem, q_tile, k_tile);           // S  = Q_i K_j^T
+          mma_s_type<D>(tmem, q_tile, tile(0, 0));           // S  = Q_i K_j^T
           tc_commit(smem_u32(&ctl->s_full));
-          mma_s_type<D>(tmem + 128, do_tile, v_tile);    // dP = dO_i V_j^T
+          mma_s_type<D>(tmem + 128, do_tile, tile(0, 1));    // dP = dO_i V_j^T
           tc_commit(smem_u32(&ctl->dp_full));
+        }
+        for (int u = 0; u < nk && ok; ++u) {
+          const bool more = u + 1 < nk;
+          if (more) {
+            ok = wait_phase(smem_u32(&ctl->p_full), u & 1, abort_flag, status);
+            if (ok)
+              ok = wait_phase(smem_u32(&ctl->ring_full[(u + 1) & 1]), ((u + 1) >> 1) & 1,
+                              abort_flag, status);
+            if (!ok) break;
+            tc_fence_after();
+            mma_s_type<D>(tmem, q_tile, tile(u + 1, 0));
+            tc_commit(smem_u32(&ctl->s_full));
+          }
           ok = wait_phase(smem_u32(&ctl->ds_full), u & 1, abort_flag, status);
           if (!ok) break;
           tc_fence_after();
-          mma_acc<D>(tmem + 256, tmem + 128, k_tile, u > 0);   // dQ += dS K_j
-          tc_commit(smem_u32(&ctl->ring_empty[s]));
+          mma_acc<D>(tmem + 256, tmem + 128, tile(u, 0), u > 0);   // dQ += dS K_j
+          tc_commit(smem_u32(&ctl->ring_empty[u & 1]));
+          if (more) {
+            mma_s_type<D>(tmem + 128, do_tile, tile(u + 1, 1));
+            tc_commit(smem_u32(&ctl->dp_full));
+          }
         }
         if (ok) tc_commit(smem_u32(&ctl->o_full));
         tc_commit(smem_u32(&ctl->drain));
@@ -607,6 +655,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       softmax_p<false, false>(t_s, args.c, nullptr, lse2_row,
                               [&](int k) { return k0 + k < n && (!CAUSAL || k0 + k <= row); },
                               any_masked, p);
+      // S has been read into registers: the tensor core may overwrite it with the next S
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full));
       ok = wait_phase(smem_u32(&ctl->dp_full), u & 1, abort_flag, status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
