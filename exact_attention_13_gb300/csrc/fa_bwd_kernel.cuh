@@ -139,10 +139,11 @@ __device__ __forceinline__ void mma_acc(uint32_t tmem_d, uint32_t tmem_a, uint32
 // the bf16 results of pass 0 land in columns 0-15 and of pass 1 in columns 16-31 of the thread's
 // range, whose fp32 values were read in pass 0.  PER_COLUMN (dK/dV kernel): column q has its own
 // LSE * log2(e) and D, read as float4 from the shared arrays; otherwise (dQ kernel) the row's
-// own values apply to every column.  `visible` masks columns when any_masked.
-template <bool PER_COLUMN, bool STORE, typename VisFn>
+// own values apply to every column.  MASKED (a separate instantiation, so the unmasked blocks
+// carry no per-column select): `visible` decides which columns keep their probability.
+template <bool PER_COLUMN, bool STORE, bool MASKED, typename VisFn>
 __device__ __forceinline__ void softmax_p(uint32_t t_s, float c, const float* l2, float l2_row,
-                                          VisFn visible, bool any_masked, float (&p)[64]) {
+                                          VisFn visible, float (&p)[64]) {
 #pragma unroll
   for (int pass = 0; pass < 2; ++pass) {
     uint32_t rs[32];
@@ -170,7 +171,7 @@ __device__ __forceinline__ void softmax_p(uint32_t t_s, float c, const float* l2
       const uint64_t x2 = fma_f32x2(f32x2(__uint_as_float(rs[i]), __uint_as_float(rs[i + 1])), c2,
                                     f32x2(-lv[i], -lv[i + 1]));
       float x0 = ex2_mufu(f32x2_lo(x2)), x1 = ex2_mufu(f32x2_hi(x2));
-      if (any_masked) {
+      if constexpr (MASKED) {
         x0 = visible(32 * pass + i) ? x0 : 0.f;
         x1 = visible(32 * pass + i + 1) ? x1 : 0.f;
       }
@@ -433,9 +434,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int q0 = qblk * kTileRows + 64 * hc;   // first query column of this half
       const bool any_masked = (CAUSAL && qblk == jblk) || (qblk + 1) * kTileRows > n;
       float p[64];
-      softmax_p<true, true>(t_s, args.c, l2, 0.f,
-                            [&](int q) { return q0 + q < n && (!CAUSAL || key <= q0 + q); },
-                            any_masked, p);
+      const auto vis = [&](int q) { return q0 + q < n && (!CAUSAL || key <= q0 + q); };
+      if (any_masked)
+        softmax_p<true, true, true>(t_s, args.c, l2, 0.f, vis, p);
+      else
+        softmax_p<true, true, false>(t_s, args.c, l2, 0.f, vis, p);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&ctl->p_full));
@@ -652,9 +655,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int k0 = u * kTileRows + 64 * hc;      // first key column of this half
       const bool any_masked = (CAUSAL && u == iblk) || (u + 1) * kTileRows > n;
       float p[64];
-      softmax_p<false, false>(t_s, args.c, nullptr, lse2_row,
-                              [&](int k) { return k0 + k < n && (!CAUSAL || k0 + k <= row); },
-                              any_masked, p);
+      const auto vis = [&](int k) { return k0 + k < n && (!CAUSAL || k0 + k <= row); };
+      if (any_masked)
+        softmax_p<false, false, true>(t_s, args.c, nullptr, lse2_row, vis, p);
+      else
+        softmax_p<false, false, false>(t_s, args.c, nullptr, lse2_row, vis, p);
       // S has been read into registers: the tensor core may overwrite it with the next S
       tc_fence_before();
       __syncwarp();
