@@ -238,13 +238,16 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   bwd_delta_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), delta, rows);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  constexpr int smem = bwd_smem_bytes<D>();
-  static_assert(smem <= 227 * 1024, "shared memory per CTA");
+  // at least 120 KB each, so that one CTA (which takes all 512 TMEM columns) runs per SM
+  constexpr int smem = bwd_smem_bytes<D>(), smem_dq = dq_smem_bytes<D>();
+  static_assert(smem <= 227 * 1024 && smem_dq <= 227 * 1024, "shared memory per CTA");
   constexpr int smem_request = smem > 120 * 1024 ? smem : 120 * 1024;
+  constexpr int smem_dq_request = smem_dq > 120 * 1024 ? smem_dq : 120 * 1024;
   static std::atomic<uint64_t> done_kv{0}, done_q{0};
   auto kkv = bwd_dkdv_kernel<D, CAUSAL>;
   auto kq = bwd_dq_kernel<D, CAUSAL>;
-  if (!set_smem_once(kkv, smem_request, dev, done_kv) || !set_smem_once(kq, smem_request, dev, done_q))
+  if (!set_smem_once(kkv, smem_request, dev, done_kv) ||
+      !set_smem_once(kq, smem_dq_request, dev, done_q))
     return FA_ERR_CUDA;
   const unsigned nblk = static_cast<unsigned>((N + kTileRows - 1) / kTileRows);
   const dim3 grid = CAUSAL ? dim3(static_cast<unsigned>(bh), nblk) : dim3(nblk, static_cast<unsigned>(bh));
@@ -254,7 +257,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   a.g0 = static_cast<__nv_bfloat16*>(dq);
   a.g1 = nullptr;
-  kq<<<grid, kBwdThreads, smem_request, stream>>>(mq, mk, mv, mdo, a);
+  kq<<<grid, kBwdThreads, smem_dq_request, stream>>>(mq, mk, mv, mdo, a);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -79,6 +79,31 @@ constexpr int bwd_smem_bytes() {
   return 6 * BwdGeo<D>::kTileBytes + static_cast<int>(sizeof(BwdCtrl)) + 1024;
 }
 
+// The dQ kernel streams K_j and V_j as separate tiles through a five-slot ring: V_j is released
+// once dP has read it and K_j once dQ has, so each load starts two to three products before it
+// is needed (a stage of both tiles, released after dQ, left one product for a 64 KB load).
+constexpr int kDqSlots = 5;
+
+struct DqCtrl {
+  uint64_t fix_full;                 // Q_i and dO_i
+  uint64_t tile_full[kDqSlots];      // tile t (K_j for t = 2j, V_j for t = 2j + 1) in slot t % 5
+  uint64_t tile_empty[kDqSlots];
+  uint64_t s_full;                   // S of the step is in TMEM
+  uint64_t dp_full;                  // dP of the step is in TMEM
+  uint64_t p_full;                   // the softmax has read S (eight warps)
+  uint64_t ds_full;                  // dS written back in bf16 (eight warps)
+  uint64_t o_full;                   // the last dQ product is done
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// two fixed tiles + the five-slot ring + the control block
+template <int D>
+constexpr int dq_smem_bytes() {
+  return (2 + kDqSlots) * BwdGeo<D>::kTileBytes + static_cast<int>(sizeof(DqCtrl)) + 1024;
+}
+
 // D_i = sum_t dO_it O_it in fp32, one warp per row.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
@@ -508,8 +533,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* s_q = smem;
   uint8_t* s_do = smem + G::kTileBytes;
-  uint8_t* s_ring = smem + 2 * G::kTileBytes;  // stage s: K at 2s, V at 2s + 1 (tiles)
-  BwdCtrl* ctl = reinterpret_cast<BwdCtrl*>(smem + 6 * G::kTileBytes);
+  uint8_t* s_ring = smem + 2 * G::kTileBytes;  // slot i at tile i
+  DqCtrl* ctl = reinterpret_cast<DqCtrl*>(smem + (2 + kDqSlots) * G::kTileBytes);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -526,9 +551,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&ctl->fix_full), 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&ctl->ring_full[s]), 1);
-      mbar_init(smem_u32(&ctl->ring_empty[s]), 1);
+    for (int i = 0; i < kDqSlots; ++i) {
+      mbar_init(smem_u32(&ctl->tile_full[i]), 1);
+      mbar_init(smem_u32(&ctl->tile_empty[i]), 1);
     }
     mbar_init(smem_u32(&ctl->s_full), 1);
     mbar_init(smem_u32(&ctl->dp_full), 1);
@@ -544,6 +569,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   int* abort_flag = &ctl->abort;
+  const int ntiles = 2 * nk;
 
   if (warp >= 8) {
     regs_dec<72>();
@@ -561,27 +587,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         bool ok = true;
         int issued = 0;
-        for (int u = 0; u < nk && ok; ++u) {
-          const int s = u & 1;
-          if (u >= 2) {
-            ok = wait_phase(smem_u32(&ctl->ring_empty[s]), ((u >> 1) - 1) & 1, abort_flag, status);
+        for (int t = 0; t < ntiles && ok; ++t) {
+          const int slot = t % kDqSlots;
+          if (t >= kDqSlots) {
+            ok = wait_phase(smem_u32(&ctl->tile_empty[slot]), (t / kDqSlots - 1) & 1, abort_flag,
+                            status);
             if (!ok) break;
           }
-          const uint32_t rb = smem_u32(&ctl->ring_full[s]);
-          mbar_arrive_expect_tx(rb, 2 * G::kTileBytes);
-          uint8_t* dk = s_ring + (2 * s) * G::kTileBytes;
-          uint8_t* dv = s_ring + (2 * s + 1) * G::kTileBytes;
-          for (int b = 0; b < G::kBoxes; ++b) {
-            tma_load_3d(smem_u32(dk + b * kTileRows * 128), &map_k, rb, b * 64, u * kTileRows, bh);
-            tma_load_3d(smem_u32(dv + b * kTileRows * 128), &map_v, rb, b * 64, u * kTileRows, bh);
-          }
+          const uint32_t tb = smem_u32(&ctl->tile_full[slot]);
+          mbar_arrive_expect_tx(tb, G::kTileBytes);
+          uint8_t* dst = s_ring + slot * G::kTileBytes;
+          const CUtensorMap* map = (t & 1) ? &map_v : &map_k;
+          for (int b = 0; b < G::kBoxes; ++b)
+            tma_load_3d(smem_u32(dst + b * kTileRows * 128), map, tb, b * 64, (t >> 1) * kTileRows,
+                        bh);
           ++issued;
         }
         if (!ok) {
+          // abort: let the copies still in flight land before the CTA's smem goes away
           wait_phase(fb, 0, abort_flag, status);
-          for (int u = issued > 2 ? issued - 2 : 0; u < issued; ++u) {
+          for (int t = issued > kDqSlots ? issued - kDqSlots : 0; t < issued; ++t) {
             const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(smem_u32(&ctl->ring_full[u & 1]), (u >> 1) & 1) &&
+            while (!mbar_try_wait(smem_u32(&ctl->tile_full[t % kDqSlots]), (t / kDqSlots) & 1) &&
                    globaltimer_ns() - t0 < kWaitLimitNs) {
             }
           }
@@ -593,38 +620,48 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         const uint32_t q_tile = smem_u32(s_q), do_tile = smem_u32(s_do);
         // Issue order per step u: S(u+1) once the softmax has read S(u), then dQ(u), dP(u+1);
-        // the tensor core computes S(u+1) while the softmax forms dS(u).
-        auto tile = [&](int u, int which) {
-          return smem_u32(s_ring + (2 * (u & 1) + which) * G::kTileBytes);
-        };
-        ok = ok && wait_phase(smem_u32(&ctl->ring_full[0]), 0, abort_flag, status);
-        if (ok) {
+        // the tensor core computes S(u+1) while the softmax forms dS(u).  V_j's slot is handed
+        // back behind dP, K_j's behind dQ.
+        auto tile = [&](int t) { return smem_u32(s_ring + (t % kDqSlots) * G::kTileBytes); };
+        auto tile_ready = [&](int t) {
+          const bool r = wait_phase(smem_u32(&ctl->tile_full[t % kDqSlots]), (t / kDqSlots) & 1,
+                                    abort_flag, status);
           tc_fence_after();
-          mma_s_type<D>(tmem, q_tile, tile(0, 0));           // S  = Q_i K_j^T
+          return r;
+        };
+        auto release = [&](int t) { tc_commit(smem_u32(&ctl->tile_empty[t % kDqSlots])); };
+        ok = ok && tile_ready(0);
+        if (ok) {
+          mma_s_type<D>(tmem, q_tile, tile(0));           // S  = Q_i K_j^T
           tc_commit(smem_u32(&ctl->s_full));
-          mma_s_type<D>(tmem + 128, do_tile, tile(0, 1));    // dP = dO_i V_j^T
+          ok = tile_ready(1);
+        }
+        if (ok) {
+          mma_s_type<D>(tmem + 128, do_tile, tile(1));    // dP = dO_i V_j^T
           tc_commit(smem_u32(&ctl->dp_full));
+          release(1);
         }
         for (int u = 0; u < nk && ok; ++u) {
           const bool more = u + 1 < nk;
           if (more) {
             ok = wait_phase(smem_u32(&ctl->p_full), u & 1, abort_flag, status);
-            if (ok)
-              ok = wait_phase(smem_u32(&ctl->ring_full[(u + 1) & 1]), ((u + 1) >> 1) & 1,
-                              abort_flag, status);
+            if (ok) ok = tile_ready(2 * u + 2);
             if (!ok) break;
             tc_fence_after();
-            mma_s_type<D>(tmem, q_tile, tile(u + 1, 0));
+            mma_s_type<D>(tmem, q_tile, tile(2 * u + 2));
             tc_commit(smem_u32(&ctl->s_full));
           }
           ok = wait_phase(smem_u32(&ctl->ds_full), u & 1, abort_flag, status);
           if (!ok) break;
           tc_fence_after();
-          mma_acc<D>(tmem + 256, tmem + 128, tile(u, 0), u > 0);   // dQ += dS K_j
-          tc_commit(smem_u32(&ctl->ring_empty[u & 1]));
+          mma_acc<D>(tmem + 256, tmem + 128, tile(2 * u), u > 0);   // dQ += dS K_j
+          release(2 * u);
           if (more) {
-            mma_s_type<D>(tmem + 128, do_tile, tile(u + 1, 1));
+            ok = tile_ready(2 * u + 3);
+            if (!ok) break;
+            mma_s_type<D>(tmem + 128, do_tile, tile(2 * u + 3));
             tc_commit(smem_u32(&ctl->dp_full));
+            release(2 * u + 3);
           }
         }
         if (ok) tc_commit(smem_u32(&ctl->o_full));
