@@ -25,7 +25,9 @@
 // bf16) from TMEM and their B operand MN-major from the same tiles.  Warp roles (384 threads):
 // warps 0-7 one half-row of S each (warp w: TMEM lanes 32 (w % 4) .., columns 64 (w / 4) ..),
 // warp 8 TMA, warp 9 MMA issue and TMEM owner, warp 10 (dK/dV only) stages LSE and D of each query
-// block in shared memory.  Every wait is bounded as in the forward kernel.
+// block in shared memory.  Every wait is bounded as in the forward kernel (and a test build with
+// EXATTN_INJECT_STALL stops each producer after the CTA's fixed tiles, so the first streamed wait
+// runs out and every role leaves through the abort path).
 #pragma once
 
 #include "fa_fwd_kernel.cuh"
@@ -322,7 +324,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         bool ok = true;
         int issued = 0;
-        for (int u = 0; u < nq && ok; ++u) {
+        const int n_stream = EXATTN_INJECT_STALL ? 0 : nq;   // test builds: stop after K_j, V_j
+        for (int u = 0; u < n_stream && ok; ++u) {
           const int s = u & 1;
           if (u >= 2) {
             ok = wait_phase(smem_u32(&ctl->ring_empty[s]), ((u >> 1) - 1) & 1, abort_flag, status);
@@ -587,7 +590,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         bool ok = true;
         int issued = 0;
-        for (int t = 0; t < ntiles && ok; ++t) {
+        const int n_load = EXATTN_INJECT_STALL ? 0 : ntiles;   // test builds: stop after Q_i, dO_i
+        for (int t = 0; t < n_load && ok; ++t) {
           const int slot = t % kDqSlots;
           if (t >= kDqSlots) {
             ok = wait_phase(smem_u32(&ctl->tile_empty[slot]), (t / kDqSlots - 1) & 1, abort_flag,
