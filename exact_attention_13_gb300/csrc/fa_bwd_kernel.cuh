@@ -139,12 +139,14 @@ __device__ __forceinline__ uint32_t p_col(int kb) { return kb < 4 ? kb * 8 : 64 
 template <int D>
 __device__ __forceinline__ void mma_s_type(uint32_t tmem_d, uint32_t a_tile, uint32_t b_tile) {
   using G = BwdGeo<D>;
+  uint64_t da[G::kKSteps], db[G::kKSteps];
 #pragma unroll
   for (int kb = 0; kb < G::kKSteps; ++kb) {
     const uint32_t off = (kb * 32 / 128) * kTileRows * 128 + (kb * 32) % 128;
-    mma_f16_ss(tmem_d, smem_desc(a_tile + off, 16, 1024, kSwizzle128B),
-               smem_desc(b_tile + off, 16, 1024, kSwizzle128B), G::kIdescS, kb > 0);
+    da[kb] = smem_desc(a_tile + off, 16, 1024, kSwizzle128B);
+    db[kb] = smem_desc(b_tile + off, 16, 1024, kSwizzle128B);
   }
+  mma_chain_ss<G::kKSteps, 0>(tmem_d, G::kIdescS, 0u, da, db);
 }
 
 // Accumulating product D += A (128 x 128 bf16 from TMEM) * B (128 x D tile, MN-major).
@@ -152,11 +154,14 @@ template <int D>
 __device__ __forceinline__ void mma_acc(uint32_t tmem_d, uint32_t tmem_a, uint32_t b_tile,
                                         bool accumulate) {
   using G = BwdGeo<D>;
+  uint32_t pa[8];
+  uint64_t db[8];
 #pragma unroll
-  for (int kb = 0; kb < 8; ++kb)
-    mma_f16_ts(tmem_d, tmem_a + p_col(kb),
-               smem_desc(b_tile + kb * 16 * 128, kTileRows * 128, 1024, kSwizzle128B),
-               G::kIdescAcc, (accumulate || kb > 0) ? 1u : 0u);
+  for (int kb = 0; kb < 8; ++kb) {
+    pa[kb] = tmem_a + p_col(kb);
+    db[kb] = smem_desc(b_tile + kb * 16 * 128, kTileRows * 128, 1024, kSwizzle128B);
+  }
+  mma_chain_ts<8, 0>(tmem_d, G::kIdescAcc, accumulate ? 1u : 0u, pa, db);
 }
 
 // Half-row softmax steps shared by both kernels, for the 64 columns of this thread's row.

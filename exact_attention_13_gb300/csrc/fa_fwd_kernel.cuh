@@ -186,6 +186,14 @@ struct Geo {
   static constexpr int kPvSwBytes = kPv16 ? 128 : kSwBytes; // swizzle span of the PV B tile
   static constexpr uint32_t kIdescS = instr_desc(128, 128, FP8 ? 0 : 1, false, false);
   static constexpr uint32_t kIdescPV = instr_desc(128, D, FP8 ? 0 : 1, false, true);
+  // descriptor offset (16-byte units) of K step kb of an S operand tile; 0 past the last step
+  __host__ __device__ static constexpr int s_off(int kb) {
+    return kb >= kKStepsS ? 0
+                          : ((kb * kKStepBytes / kSwBytes) * kTileRows * kSwBytes +
+                             (kb * kKStepBytes) % kSwBytes) >> 4;
+  }
+  // descriptor step (16-byte units) between the V key groups of consecutive PV MMAs
+  static constexpr int kPvStep = (kKeysPerPv * kPvSwBytes) >> 4;
 };
 
 // Shared-memory control block (after the operand tiles).
@@ -455,94 +463,95 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t ring_base = smem_u32(s_ring);
       const int nkv[2] = {nkv0, nkv1};
 
+      // The tensor core holds only a couple of MMAs in its queue, so any time this thread spends
+      // between two products (waits, descriptor arithmetic, issue slots lost to the softmax
+      // warps of its SMSP) leaves the pipe idle.  Each step therefore does its waits first, then
+      // issues P V and the next S back to back with descriptors formed from per-tile bases.
       auto wait_kv = [&](int t) -> bool {
-        const bool r = wait_phase(smem_u32(&ctl->kv_full[t % G::kSlots]),
-                                  (t / G::kSlots) & 1, abort_flag, args.status);
-        tc_fence_after();
-        return r;
+        return wait_phase(smem_u32(&ctl->kv_full[t % G::kSlots]), (t / G::kSlots) & 1,
+                          abort_flag, args.status);
       };
-      // S_h = Q_h K_j^T into TMEM columns [128h, 128h + 128)
-      auto issue_s = [&](int h, int j) -> bool {
+      const uint64_t q_desc = smem_desc(q_base, 16, 8 * G::kSwBytes, G::kSwMode);
+      const uint64_t ring_desc = smem_desc(ring_base, 16, 8 * G::kSwBytes, G::kSwMode);
+      // S_h = Q_h K_j^T into TMEM columns [128h, 128h + 128); K_j has landed
+      auto issue_s = [&](int h, int j) {
         const int t = 2 * j;
-        if (!wait_kv(t)) return false;
-        EXATTN_TRACE_EVENT(7, h, j);
-        const uint32_t k_tile = ring_base + (t % G::kSlots) * G::kTileBytes;
-        const uint32_t q_tile = q_base + h * G::kTileBytes;
-#pragma unroll
-        for (int kb = 0; kb < G::kKStepsS; ++kb) {
-          const uint32_t off = (kb * G::kKStepBytes / G::kSwBytes) * kTileRows * G::kSwBytes +
-                               (kb * G::kKStepBytes) % G::kSwBytes;
-          const uint64_t da = smem_desc(q_tile + off, 16, 8 * G::kSwBytes, G::kSwMode);
-          const uint64_t db = smem_desc(k_tile + off, 16, 8 * G::kSwBytes, G::kSwMode);
-          if constexpr (FP8)
-            mma_f8_ss(tmem + h * 128, da, db, G::kIdescS, kb > 0);
-          else
-            mma_f16_ss(tmem + h * 128, da, db, G::kIdescS, kb > 0);
-        }
+        const uint64_t qd = q_desc + static_cast<uint64_t>(h * (G::kTileBytes >> 4));
+        const uint64_t kd = ring_desc + static_cast<uint64_t>((t % G::kSlots) * (G::kTileBytes >> 4));
+        mma_chain_ss_off<G::kKStepsS, FP8 ? 1 : 0, G::s_off(1), G::s_off(2), G::s_off(3),
+                         G::s_off(4), G::s_off(5), G::s_off(6), G::s_off(7)>(
+            tmem + h * 128, G::kIdescS, 0u, qd, kd);
         tc_commit(smem_u32(&ctl->s_full[h]));
         EXATTN_TRACE_EVENT(6, h, j);
         const bool last_user = (h == 1) || (j >= nkv[1]);
         if (last_user) tc_commit(smem_u32(&ctl->kv_empty[t % G::kSlots]));
-        return true;
       };
-      // O_h += P_h V_j, P_h read from TMEM over S_h's columns.  The softmax publishes P in two
-      // halves of 64 keys; the MMAs of the first half start while the second is computed.
-      auto issue_pv = [&](int h, int j) -> bool {
+      // V_j (or its f16 copy) ready; returns its shared-memory descriptor base
+      auto wait_v = [&](int h, int j, uint64_t& vd) -> bool {
         const int t = 2 * j + 1;
-        uint32_t v_tile;
         if constexpr (G::kPv16) {
           if (!wait_phase(smem_u32(&ctl->v16_full[j & 1]), (j >> 1) & 1, abort_flag,
                           args.status))
             return false;
-          tc_fence_after();
-          v_tile = smem_u32(s_v16) + (j & 1) * G::kV16TileBytes;
+          vd = smem_desc(smem_u32(s_v16) + (j & 1) * G::kV16TileBytes, kTileRows * G::kPvSwBytes,
+                         8 * G::kPvSwBytes, kSwizzle128B);
           // both converter warps are done with the e4m3 copy: hand its slot back
           const bool first_user = (h == 0) || (j >= nkv[0]);
           if (first_user) mbar_arrive(smem_u32(&ctl->kv_empty[t % G::kSlots]));
         } else {
           if (!wait_kv(t)) return false;
-          v_tile = ring_base + (t % G::kSlots) * G::kTileBytes;
+          vd = smem_desc(ring_base + (t % G::kSlots) * G::kTileBytes, kTileRows * G::kPvSwBytes,
+                         8 * G::kPvSwBytes, G::kSwMode);
         }
         EXATTN_TRACE_EVENT(8, h, j);
+        return true;
+      };
+      // O_h += P_h V_j, P_h read from TMEM over S_h's columns.  The softmax may publish P in two
+      // halves of 64 keys; the MMAs of the first half start while the second is computed.
+      auto issue_pv_part = [&](int h, int j, int half, uint64_t vd) {
+        constexpr int kN = G::kPvSteps / kPHalves;   // MMAs per published part of P
+        // A: 8 TMEM columns of P per MMA; B: the next key group of V
+        mma_chain_ts_off<kN, G::kPE4m3 ? 1 : 0, G::kPvStep, 8, 16, 24, 32, 40, 48, 56>(
+            tmem + 256 + h * 128, G::kIdescPV, (j > 0 || half > 0) ? 1u : 0u,
+            tmem + h * 128 + half * kN * 8,
+            vd + static_cast<uint64_t>(half * kN * G::kPvStep));
+      };
+      // one step of tile h: P V of block j, then S of block j + 1 (which overwrites P_h)
+      auto step = [&](int h, int j) -> bool {
+        const bool more = j + 1 < nkv[h];
+        uint64_t vd;
+        if (!wait_v(h, j, vd)) return false;
+        if (more && !wait_kv(2 * (j + 1))) return false;
+        EXATTN_TRACE_EVENT(7, h, j + 1);
 #pragma unroll
         for (int half = 0; half < kPHalves; ++half) {
           if (!wait_phase(smem_u32(&ctl->p_full[h][half]), j & 1, abort_flag, args.status))
             return false;
           tc_fence_after();
           if (half == 0) EXATTN_TRACE_EVENT(4, h, j);
-#pragma unroll
-          for (int kk = 0; kk < G::kPvSteps / kPHalves; ++kk) {
-            const int kb = half * (G::kPvSteps / kPHalves) + kk;
-            const uint64_t dv =
-                smem_desc(v_tile + kb * G::kKeysPerPv * G::kPvSwBytes, kTileRows * G::kPvSwBytes,
-                          8 * G::kPvSwBytes, G::kPv16 ? kSwizzle128B : G::kSwMode);
-            const uint32_t a = tmem + h * 128 + kb * 8;
-            const uint32_t acc = (j > 0 || kb > 0) ? 1u : 0u;
-            if constexpr (G::kPE4m3)
-              mma_f8_ts(tmem + 256 + h * 128, a, dv, G::kIdescPV, acc);
-            else
-              mma_f16_ts(tmem + 256 + h * 128, a, dv, G::kIdescPV, acc);
-          }
+          issue_pv_part(h, j, half, vd);
         }
         EXATTN_TRACE_EVENT(5, h, j);
         if (j == nkv[h] - 1) tc_commit(smem_u32(&ctl->o_full[h]));
         const bool last_user = (h == 1) || (j >= nkv[1]);
         // PV16: the converter has already released the e4m3 slot; free the f16 copy instead
         if (last_user)
-          tc_commit(smem_u32(G::kPv16 ? &ctl->v16_empty[j & 1] : &ctl->kv_empty[t % G::kSlots]));
+          tc_commit(smem_u32(G::kPv16 ? &ctl->v16_empty[j & 1]
+                                      : &ctl->kv_empty[(2 * j + 1) % G::kSlots]));
+        if (more) issue_s(h, j + 1);
         return true;
       };
 
-      if (ok && nkv0 > 0) ok = issue_s(0, 0);
-      if (ok && nkv1 > 0) ok = issue_s(1, 0);
+      ok = ok && wait_kv(0);
+      if (ok) {
+        tc_fence_after();
+        if (nkv0 > 0) issue_s(0, 0);
+        if (nkv1 > 0) issue_s(1, 0);
+      }
       for (int j = 0; j < nkv_load && ok; ++j) {
 #pragma unroll
-        for (int h = 0; h < 2 && ok; ++h) {
-          if (j < nkv[h]) {
-            ok = issue_pv(h, j);
-            if (ok && j + 1 < nkv[h]) ok = issue_s(h, j + 1);
-          }
-        }
+        for (int h = 0; h < 2 && ok; ++h)
+          if (j < nkv[h]) ok = step(h, j);
       }
       // make sure nothing this thread issued is still running before TMEM is released
       tc_commit(smem_u32(&ctl->drain));

@@ -226,6 +226,402 @@ __device__ __forceinline__ void mma_f8_ts(uint32_t d, uint32_t a_tmem, uint64_t 
       : "memory");
 }
 
+// ---- MMA chains: all MMAs of one product in a single asm block, descriptors precomputed.
+// Issued this way the tensor core runs the attention kernel's S / P V alternation at its full
+// rate (64 cycles per 128x128x16 bf16 MMA, measured); the same MMAs issued one asm statement at
+// a time ran at 92-113 cycles.  The first MMA accumulates into D when acc0 != 0, the others
+// always accumulate.  KIND: 0 = kind::f16, 1 = kind::f8f6f4.
+
+template <int KIND>
+__device__ __forceinline__ void mma_chain_ss2(uint32_t d, uint32_t idesc, uint32_t acc0,
+                                               const uint64_t (&a)[2], const uint64_t (&b)[2]) {
+  if constexpr (KIND == 0) {
+    asm volatile(
+      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %5, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %6, %1, t;\n\t"
+      "}" ::"r"(d), "r"(idesc), "r"(acc0), "l"(a[0]), "l"(a[1]), "l"(b[0]), "l"(b[1])
+      : "memory");
+  } else {
+    asm volatile(
+      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, %5, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %4, %6, %1, t;\n\t"
+      "}" ::"r"(d), "r"(idesc), "r"(acc0), "l"(a[0]), "l"(a[1]), "l"(b[0]), "l"(b[1])
+      : "memory");
+  }
+}
+
+template <int KIND>
+__device__ __forceinline__ void mma_chain_ss4(uint32_t d, uint32_t idesc, uint32_t acc0,
+                                               const uint64_t (&a)[4], const uint64_t (&b)[4]) {
+  if constexpr (KIND == 0) {
+    asm volatile(
+      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %9, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %10, %1, t;\n\t"
+      "}" ::"r"(d), "r"(idesc), "r"(acc0), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3])
+      : "memory");
+  } else {
+    asm volatile(
+      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, %7, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %4, %8, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %5, %9, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %6, %10, %1, t;\n\t"
+      "}" ::"r"(d), "r"(idesc), "r"(acc0), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3])
+      : "memory");
+  }
+}
+
+template <int KIND>
+__device__ __forceinline__ void mma_chain_ss8(uint32_t d, uint32_t idesc, uint32_t acc0,
+                                               const uint64_t (&a)[8], const uint64_t (&b)[8]) {
+  if constexpr (KIND == 0) {
+    asm volatile(
+      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %17, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %10, %18, %1, t;\n\t"
+      "}" ::"r"(d), "r"(idesc), "r"(acc0), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7])
+      : "memory");
+  } else {
+    asm volatile(
+      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, %11, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %4, %12, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %5, %13, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %6, %14, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %7, %15, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %8, %16, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %9, %17, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %10, %18, %1, t;\n\t"
+      "}" ::"r"(d), "r"(idesc), "r"(acc0), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7])
+      : "memory");
+  }
+}
+
+template <int KIND>
+__device__ __forceinline__ void mma_chain_ts2(uint32_t d, uint32_t idesc, uint32_t acc0,
+                                               const uint32_t (&a)[2], const uint64_t (&b)[2]) {
+  if constexpr (KIND == 0) {
+    asm volatile(
+      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %5, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %6, %1, t;\n\t"
+      "}" ::"r"(d), "r"(idesc), "r"(acc0), "r"(a[0]), "r"(a[1]), "l"(b[0]), "l"(b[1])
+      : "memory");
+  } else {
+    asm volatile(
+      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%3], %5, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%4], %6, %1, t;\n\t"
+      "}" ::"r"(d), "r"(idesc), "r"(acc0), "r"(a[0]), "r"(a[1]), "l"(b[0]), "l"(b[1])
+      : "memory");
+  }
+}
+
+template <int KIND>
+__device__ __forceinline__ void mma_chain_ts4(uint32_t d, uint32_t idesc, uint32_t acc0,
+                                               const uint32_t (&a)[4], const uint64_t (&b)[4]) {
+  if constexpr (KIND == 0) {
+    asm volatile(
+      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %7, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %8, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %9, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %10, %1, t;\n\t"
+      "}" ::"r"(d), "r"(idesc), "r"(acc0), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3])
+      : "memory");
+  } else {
+    asm volatile(
+      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%3], %7, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%4], %8, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%5], %9, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%6], %10, %1, t;\n\t"
+      "}" ::"r"(d), "r"(idesc), "r"(acc0), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3])
+      : "memory");
+  }
+}
+
+template <int KIND>
+__device__ __forceinline__ void mma_chain_ts8(uint32_t d, uint32_t idesc, uint32_t acc0,
+                                               const uint32_t (&a)[8], const uint64_t (&b)[8]) {
+  if constexpr (KIND == 0) {
+    asm volatile(
+      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %11, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %12, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %13, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %14, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %15, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %16, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %17, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%10], %18, %1, t;\n\t"
+      "}" ::"r"(d), "r"(idesc), "r"(acc0), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7])
+      : "memory");
+  } else {
+    asm volatile(
+      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%3], %11, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%4], %12, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%5], %13, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%6], %14, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%7], %15, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%8], %16, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%9], %17, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%10], %18, %1, t;\n\t"
+      "}" ::"r"(d), "r"(idesc), "r"(acc0), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7])
+      : "memory");
+  }
+}
+
+// Chain of N (2, 4 or 8) MMAs: A from shared memory (ss) or tensor memory (ts).
+template <int N, int KIND>
+__device__ __forceinline__ void mma_chain_ss(uint32_t d, uint32_t idesc, uint32_t acc0,
+                                             const uint64_t (&a)[N], const uint64_t (&b)[N]) {
+  static_assert(N == 2 || N == 4 || N == 8, "MMA chain length");
+  if constexpr (N == 2)
+    mma_chain_ss2<KIND>(d, idesc, acc0, a, b);
+  else if constexpr (N == 4)
+    mma_chain_ss4<KIND>(d, idesc, acc0, a, b);
+  else
+    mma_chain_ss8<KIND>(d, idesc, acc0, a, b);
+}
+
+template <int N, int KIND>
+__device__ __forceinline__ void mma_chain_ts(uint32_t d, uint32_t idesc, uint32_t acc0,
+                                             const uint32_t (&a)[N], const uint64_t (&b)[N]) {
+  static_assert(N == 2 || N == 4 || N == 8, "MMA chain length");
+  if constexpr (N == 2)
+    mma_chain_ts2<KIND>(d, idesc, acc0, a, b);
+  else if constexpr (N == 4)
+    mma_chain_ts4<KIND>(d, idesc, acc0, a, b);
+  else
+    mma_chain_ts8<KIND>(d, idesc, acc0, a, b);
+}
+
+// ---- MMA chains from base descriptors: the per-MMA descriptors are the base plus immediate
+// offsets (template arguments, in 16-byte units for shared-memory descriptors and in columns
+// for tensor-memory A operands), formed inside the asm block, so only the bases occupy
+// registers in the issuing thread.  Offsets of MMAs past N are ignored.
+
+template <int N, int KIND, int O1, int O2, int O3, int O4, int O5, int O6, int O7>
+__device__ __forceinline__ void mma_chain_ss_off(uint32_t d, uint32_t idesc, uint32_t acc0, uint64_t a,
+                                                  uint64_t b) {
+  static_assert(N == 2 || N == 4 || N == 8, "MMA chain length");
+  if constexpr (N == 2 && KIND == 0) {
+    asm volatile(
+      "{\n\t.reg .pred p, t; .reg .b64 a1; .reg .b64 b1;\n\t"
+      "setp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "add.s64 a1, %3, %5;\n\tadd.s64 b1, %4, %5;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %4, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %1, t;\n\t"
+      "}"
+      :: "r"(d), "r"(idesc), "r"(acc0), "l"(a), "l"(b), "n"(O1)
+      : "memory");
+  }
+  if constexpr (N == 2 && KIND == 1) {
+    asm volatile(
+      "{\n\t.reg .pred p, t; .reg .b64 a1; .reg .b64 b1;\n\t"
+      "setp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "add.s64 a1, %3, %5;\n\tadd.s64 b1, %4, %5;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, %4, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a1, b1, %1, t;\n\t"
+      "}"
+      :: "r"(d), "r"(idesc), "r"(acc0), "l"(a), "l"(b), "n"(O1)
+      : "memory");
+  }
+  if constexpr (N == 4 && KIND == 0) {
+    asm volatile(
+      "{\n\t.reg .pred p, t; .reg .b64 a1, a2, a3; .reg .b64 b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "add.s64 a1, %3, %5;\n\tadd.s64 b1, %4, %5;\n\t"
+      "add.s64 a2, %3, %6;\n\tadd.s64 b2, %4, %6;\n\t"
+      "add.s64 a3, %3, %7;\n\tadd.s64 b3, %4, %7;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %4, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %1, t;\n\t"
+      "}"
+      :: "r"(d), "r"(idesc), "r"(acc0), "l"(a), "l"(b), "n"(O1), "n"(O2), "n"(O3)
+      : "memory");
+  }
+  if constexpr (N == 4 && KIND == 1) {
+    asm volatile(
+      "{\n\t.reg .pred p, t; .reg .b64 a1, a2, a3; .reg .b64 b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "add.s64 a1, %3, %5;\n\tadd.s64 b1, %4, %5;\n\t"
+      "add.s64 a2, %3, %6;\n\tadd.s64 b2, %4, %6;\n\t"
+      "add.s64 a3, %3, %7;\n\tadd.s64 b3, %4, %7;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, %4, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a1, b1, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a2, b2, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a3, b3, %1, t;\n\t"
+      "}"
+      :: "r"(d), "r"(idesc), "r"(acc0), "l"(a), "l"(b), "n"(O1), "n"(O2), "n"(O3)
+      : "memory");
+  }
+  if constexpr (N == 8 && KIND == 0) {
+    asm volatile(
+      "{\n\t.reg .pred p, t; .reg .b64 a1, a2, a3, a4, a5, a6, a7; .reg .b64 b1, b2, b3, b4, b5, b6, b7;\n\t"
+      "setp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "add.s64 a1, %3, %5;\n\tadd.s64 b1, %4, %5;\n\t"
+      "add.s64 a2, %3, %6;\n\tadd.s64 b2, %4, %6;\n\t"
+      "add.s64 a3, %3, %7;\n\tadd.s64 b3, %4, %7;\n\t"
+      "add.s64 a4, %3, %8;\n\tadd.s64 b4, %4, %8;\n\t"
+      "add.s64 a5, %3, %9;\n\tadd.s64 b5, %4, %9;\n\t"
+      "add.s64 a6, %3, %10;\n\tadd.s64 b6, %4, %10;\n\t"
+      "add.s64 a7, %3, %11;\n\tadd.s64 b7, %4, %11;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %4, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a4, b4, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a5, b5, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a6, b6, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a7, b7, %1, t;\n\t"
+      "}"
+      :: "r"(d), "r"(idesc), "r"(acc0), "l"(a), "l"(b), "n"(O1), "n"(O2), "n"(O3), "n"(O4), "n"(O5), "n"(O6), "n"(O7)
+      : "memory");
+  }
+  if constexpr (N == 8 && KIND == 1) {
+    asm volatile(
+      "{\n\t.reg .pred p, t; .reg .b64 a1, a2, a3, a4, a5, a6, a7; .reg .b64 b1, b2, b3, b4, b5, b6, b7;\n\t"
+      "setp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "add.s64 a1, %3, %5;\n\tadd.s64 b1, %4, %5;\n\t"
+      "add.s64 a2, %3, %6;\n\tadd.s64 b2, %4, %6;\n\t"
+      "add.s64 a3, %3, %7;\n\tadd.s64 b3, %4, %7;\n\t"
+      "add.s64 a4, %3, %8;\n\tadd.s64 b4, %4, %8;\n\t"
+      "add.s64 a5, %3, %9;\n\tadd.s64 b5, %4, %9;\n\t"
+      "add.s64 a6, %3, %10;\n\tadd.s64 b6, %4, %10;\n\t"
+      "add.s64 a7, %3, %11;\n\tadd.s64 b7, %4, %11;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, %4, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a1, b1, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a2, b2, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a3, b3, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a4, b4, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a5, b5, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a6, b6, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a7, b7, %1, t;\n\t"
+      "}"
+      :: "r"(d), "r"(idesc), "r"(acc0), "l"(a), "l"(b), "n"(O1), "n"(O2), "n"(O3), "n"(O4), "n"(O5), "n"(O6), "n"(O7)
+      : "memory");
+  }
+}
+
+template <int N, int KIND, int BSTEP, int O1, int O2, int O3, int O4, int O5, int O6, int O7>
+__device__ __forceinline__ void mma_chain_ts_off(uint32_t d, uint32_t idesc, uint32_t acc0, uint32_t a,
+                                                  uint64_t b) {
+  static_assert(N == 2 || N == 4 || N == 8, "MMA chain length");
+  if constexpr (N == 2 && KIND == 0) {
+    asm volatile(
+      "{\n\t.reg .pred p, t; .reg .b32 a1; .reg .b64 b1;\n\t"
+      "setp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "add.u32 a1, %3, %5;\n\tadd.s64 b1, %4, %6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %4, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %1, t;\n\t"
+      "}"
+      :: "r"(d), "r"(idesc), "r"(acc0), "r"(a), "l"(b), "n"(O1), "n"(1 * BSTEP)
+      : "memory");
+  }
+  if constexpr (N == 2 && KIND == 1) {
+    asm volatile(
+      "{\n\t.reg .pred p, t; .reg .b32 a1; .reg .b64 b1;\n\t"
+      "setp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "add.u32 a1, %3, %5;\n\tadd.s64 b1, %4, %6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%3], %4, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a1], b1, %1, t;\n\t"
+      "}"
+      :: "r"(d), "r"(idesc), "r"(acc0), "r"(a), "l"(b), "n"(O1), "n"(1 * BSTEP)
+      : "memory");
+  }
+  if constexpr (N == 4 && KIND == 0) {
+    asm volatile(
+      "{\n\t.reg .pred p, t; .reg .b32 a1, a2, a3; .reg .b64 b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "add.u32 a1, %3, %5;\n\tadd.s64 b1, %4, %8;\n\t"
+      "add.u32 a2, %3, %6;\n\tadd.s64 b2, %4, %9;\n\t"
+      "add.u32 a3, %3, %7;\n\tadd.s64 b3, %4, %10;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %4, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %1, t;\n\t"
+      "}"
+      :: "r"(d), "r"(idesc), "r"(acc0), "r"(a), "l"(b), "n"(O1), "n"(O2), "n"(O3), "n"(1 * BSTEP), "n"(2 * BSTEP), "n"(3 * BSTEP)
+      : "memory");
+  }
+  if constexpr (N == 4 && KIND == 1) {
+    asm volatile(
+      "{\n\t.reg .pred p, t; .reg .b32 a1, a2, a3; .reg .b64 b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "add.u32 a1, %3, %5;\n\tadd.s64 b1, %4, %8;\n\t"
+      "add.u32 a2, %3, %6;\n\tadd.s64 b2, %4, %9;\n\t"
+      "add.u32 a3, %3, %7;\n\tadd.s64 b3, %4, %10;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%3], %4, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a1], b1, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a2], b2, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a3], b3, %1, t;\n\t"
+      "}"
+      :: "r"(d), "r"(idesc), "r"(acc0), "r"(a), "l"(b), "n"(O1), "n"(O2), "n"(O3), "n"(1 * BSTEP), "n"(2 * BSTEP), "n"(3 * BSTEP)
+      : "memory");
+  }
+  if constexpr (N == 8 && KIND == 0) {
+    asm volatile(
+      "{\n\t.reg .pred p, t; .reg .b32 a1, a2, a3, a4, a5, a6, a7; .reg .b64 b1, b2, b3, b4, b5, b6, b7;\n\t"
+      "setp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "add.u32 a1, %3, %5;\n\tadd.s64 b1, %4, %12;\n\t"
+      "add.u32 a2, %3, %6;\n\tadd.s64 b2, %4, %13;\n\t"
+      "add.u32 a3, %3, %7;\n\tadd.s64 b3, %4, %14;\n\t"
+      "add.u32 a4, %3, %8;\n\tadd.s64 b4, %4, %15;\n\t"
+      "add.u32 a5, %3, %9;\n\tadd.s64 b5, %4, %16;\n\t"
+      "add.u32 a6, %3, %10;\n\tadd.s64 b6, %4, %17;\n\t"
+      "add.u32 a7, %3, %11;\n\tadd.s64 b7, %4, %18;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %4, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], b4, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a5], b5, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], b6, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a7], b7, %1, t;\n\t"
+      "}"
+      :: "r"(d), "r"(idesc), "r"(acc0), "r"(a), "l"(b), "n"(O1), "n"(O2), "n"(O3), "n"(O4), "n"(O5), "n"(O6), "n"(O7), "n"(1 * BSTEP), "n"(2 * BSTEP), "n"(3 * BSTEP), "n"(4 * BSTEP), "n"(5 * BSTEP), "n"(6 * BSTEP), "n"(7 * BSTEP)
+      : "memory");
+  }
+  if constexpr (N == 8 && KIND == 1) {
+    asm volatile(
+      "{\n\t.reg .pred p, t; .reg .b32 a1, a2, a3, a4, a5, a6, a7; .reg .b64 b1, b2, b3, b4, b5, b6, b7;\n\t"
+      "setp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "add.u32 a1, %3, %5;\n\tadd.s64 b1, %4, %12;\n\t"
+      "add.u32 a2, %3, %6;\n\tadd.s64 b2, %4, %13;\n\t"
+      "add.u32 a3, %3, %7;\n\tadd.s64 b3, %4, %14;\n\t"
+      "add.u32 a4, %3, %8;\n\tadd.s64 b4, %4, %15;\n\t"
+      "add.u32 a5, %3, %9;\n\tadd.s64 b5, %4, %16;\n\t"
+      "add.u32 a6, %3, %10;\n\tadd.s64 b6, %4, %17;\n\t"
+      "add.u32 a7, %3, %11;\n\tadd.s64 b7, %4, %18;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%3], %4, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a1], b1, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a2], b2, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a3], b3, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a4], b4, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a5], b5, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a6], b6, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a7], b7, %1, t;\n\t"
+      "}"
+      :: "r"(d), "r"(idesc), "r"(acc0), "r"(a), "l"(b), "n"(O1), "n"(O2), "n"(O3), "n"(O4), "n"(O5), "n"(O6), "n"(O7), "n"(1 * BSTEP), "n"(2 * BSTEP), "n"(3 * BSTEP), "n"(4 * BSTEP), "n"(5 * BSTEP), "n"(6 * BSTEP), "n"(7 * BSTEP)
+      : "memory");
+  }
+}
+
 // ---- TMEM <-> registers, shape 32x32b: thread t of the warp owns lane (base + t), and each
 // .xN moves N consecutive 32-bit columns.
 #define EXATTN_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
