@@ -483,8 +483,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem + h * 128, G::kIdescS, 0u, qd, kd);
         tc_commit(smem_u32(&ctl->s_full[h]));
         EXATTN_TRACE_EVENT(6, h, j);
-        const bool last_user = (h == 1) || (j >= nkv[1]);
-        if (last_user) tc_commit(smem_u32(&ctl->kv_empty[t % G::kSlots]));
       };
       // V_j (or its f16 copy) ready; returns its shared-memory descriptor base
       auto wait_v = [&](int h, int j, uint64_t& vd) -> bool {
@@ -533,11 +531,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         EXATTN_TRACE_EVENT(5, h, j);
         if (j == nkv[h] - 1) tc_commit(smem_u32(&ctl->o_full[h]));
-        const bool last_user = (h == 1) || (j >= nkv[1]);
-        // PV16: the converter has already released the e4m3 slot; free the f16 copy instead
-        if (last_user)
-          tc_commit(smem_u32(G::kPv16 ? &ctl->v16_empty[j & 1]
-                                      : &ctl->kv_empty[(2 * j + 1) % G::kSlots]));
         if (more) issue_s(h, j + 1);
         return true;
       };
@@ -669,6 +662,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       if (threadIdx.x % 128 == 0) EXATTN_TRACE_EVENT(0, h, j);
+      // Ring slots go back to the producer from here rather than by tcgen05.commit from the MMA
+      // thread, whose commits would sit between two products.  Tile 1 (tile 0 when tile 1 has
+      // no rows) visits every loaded block, and its MMAs are issued after tile 0's, so S_h(j)
+      // complete means both tiles are done with K_j, and (S_h(j) following P V of block j - 1)
+      // with V_{j-1} (or its f16 copy).
+      if (threadIdx.x % 128 == 0 && h == (nkv1 > 0 ? 1 : 0)) {
+        mbar_arrive(smem_u32(&ctl->kv_empty[(2 * j) % G::kSlots]));
+        if (j > 0)
+          mbar_arrive(smem_u32(G::kPv16 ? &ctl->v16_empty[(j - 1) & 1]
+                                        : &ctl->kv_empty[(2 * j - 1) % G::kSlots]));
+      }
 
       // the row of S: four TMEM loads in flight, one wait
       float s[128];
