@@ -130,38 +130,31 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __r
   if (lane == 0) delta[row] = acc;
 }
 
-// TMEM column of the A operand for k-step kb of an accumulating product: the softmax warps of
-// column half 0 write their 64 bf16 values to columns [0, 32), those of half 1 to [64, 96), each
-// inside the S columns it read itself (so no warp overwrites S another warp has not read yet).
-__device__ __forceinline__ uint32_t p_col(int kb) { return kb < 4 ? kb * 8 : 64 + (kb - 4) * 8; }
+// A operand of an accumulating product: the softmax warps of column half 0 write their 64 bf16
+// values to TMEM columns [0, 32), those of half 1 to [64, 96), each inside the S columns it read
+// itself (so no warp overwrites S another warp has not read yet); k-step kb (16 keys) reads 8
+// columns at kb < 4 ? 8 kb : 64 + 8 (kb - 4).
 
-// S-type product into TMEM columns [col, col + 128): A and B both 128 x D K-major tiles.
+// S-type product into TMEM columns [col, col + 128): A and B both 128 x D K-major tiles.  The
+// K steps of 32 bytes advance 2 descriptor units inside a 128-byte swizzle span and 1024 units
+// (one 128-row box) past it.
 template <int D>
 __device__ __forceinline__ void mma_s_type(uint32_t tmem_d, uint32_t a_tile, uint32_t b_tile) {
   using G = BwdGeo<D>;
-  uint64_t da[G::kKSteps], db[G::kKSteps];
-#pragma unroll
-  for (int kb = 0; kb < G::kKSteps; ++kb) {
-    const uint32_t off = (kb * 32 / 128) * kTileRows * 128 + (kb * 32) % 128;
-    da[kb] = smem_desc(a_tile + off, 16, 1024, kSwizzle128B);
-    db[kb] = smem_desc(b_tile + off, 16, 1024, kSwizzle128B);
-  }
-  mma_chain_ss<G::kKSteps, 0>(tmem_d, G::kIdescS, 0u, da, db);
+  mma_chain_ss_off<G::kKSteps, 0, 2, 4, 6, 1024, 1026, 1028, 1030>(
+      tmem_d, G::kIdescS, 0u, smem_desc(a_tile, 16, 1024, kSwizzle128B),
+      smem_desc(b_tile, 16, 1024, kSwizzle128B));
 }
 
-// Accumulating product D += A (128 x 128 bf16 from TMEM) * B (128 x D tile, MN-major).
+// Accumulating product D += A (128 x 128 bf16 from TMEM, columns as above) * B (128 x D tile,
+// MN-major, 16 keys = 128 descriptor units per step).
 template <int D>
 __device__ __forceinline__ void mma_acc(uint32_t tmem_d, uint32_t tmem_a, uint32_t b_tile,
                                         bool accumulate) {
   using G = BwdGeo<D>;
-  uint32_t pa[8];
-  uint64_t db[8];
-#pragma unroll
-  for (int kb = 0; kb < 8; ++kb) {
-    pa[kb] = tmem_a + p_col(kb);
-    db[kb] = smem_desc(b_tile + kb * 16 * 128, kTileRows * 128, 1024, kSwizzle128B);
-  }
-  mma_chain_ts<8, 0>(tmem_d, G::kIdescAcc, accumulate ? 1u : 0u, pa, db);
+  mma_chain_ts_off<8, 0, 128, 8, 16, 24, 64, 72, 80, 88>(
+      tmem_d, G::kIdescAcc, accumulate ? 1u : 0u, tmem_a,
+      smem_desc(b_tile, kTileRows * 128, 1024, kSwizzle128B));
 }
 
 // Half-row softmax steps shared by both kernels, for the 64 columns of this thread's row.
