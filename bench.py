@@ -104,11 +104,13 @@ class ClockSampler:
                 "power_w_max": pmax, "samples": len(loaded), "reasons": reasons}
 
 
-def oracle_sample_rate(inp, w, target_s: float):
+def oracle_sample_rate(inp, w, target_s: float, rerun=None):
     """Time the fp64 oracle on a sample of the workload sized for about target_s seconds.
 
     The sample is a set of query rows (spread over the sequence) of the first heads; the rate is
-    the attention-forward flops of those rows (4 * keys * d each) per second, in TFLOPS.
+    the attention-forward flops of those rows (4 * keys * d each) per second, in TFLOPS.  With
+    a list as `rerun`, a callable that runs the same sample again (returning TFLOPS, seconds) is
+    appended to it.
     """
     from oracle import oracle
 
@@ -134,15 +136,21 @@ def oracle_sample_rate(inp, w, target_s: float):
 
     heads, nrows = min(bh, 2), min(len(rows_all), 256)
     tf, dt, nh, nr = run(heads, nrows)
-    # grow rows first, then heads, to reach the target duration
+    # grow rows first, then heads, to reach the target duration; shrink rows if one probe
+    # already takes longer than the target
     scale = target_s / max(dt, 1e-3)
     if scale > 1.2:
         nrows = min(len(rows_all), int(nrows * scale))
         scale /= nrows / max(nr, 1)
         heads = min(bh, max(heads, int(heads * max(scale, 1.0))))
         tf, dt, nh, nr = run(heads, nrows)
+    elif scale < 0.8:
+        heads, nrows = 1, max(1, int(nrows * scale * 2))
+        tf, dt, nh, nr = run(heads, nrows)
     sample = (f"{nr} query rows x {nh} heads of {w.name} "
               f"({'causal' if w.causal else 'all'} keys each), fp64 on {cores} threads")
+    if rerun is not None:
+        rerun.append(lambda: run(heads, nrows)[:2])
     return tf, dt, cores, sample
 
 
@@ -216,10 +224,14 @@ def run_reference(args, w, world, rank):
     if rank != 0:
         return
     inp = make_inputs(w)
+    # every step runs the same bounded sample, sized so that the whole run (warm-up included)
+    # takes about --ref-budget-s of oracle work
+    per_step = max(0.02, min(args.ref_step_s, args.ref_budget_s / (args.warmup + args.steps)))
+    rerun = []
+    _, _, cores, sample = oracle_sample_rate(inp, w, target_s=per_step, rerun=rerun)
     rates, times = [], []
-    cores, sample = None, None
     for step in range(args.warmup + args.steps):
-        tf, dt, cores, sample = oracle_sample_rate(inp, w, target_s=args.ref_step_s)
+        tf, dt = rerun[0]()
         if step >= args.warmup:
             rates.append(tf)
             times.append(dt)
@@ -560,7 +572,10 @@ def main():
     ap.add_argument("--splits", type=int, default=1,
                     help="key splits per query tile (split-KV + merge kernel)")
     ap.add_argument("--cpu-s", type=float, default=12.0, help="seconds of oracle work")
-    ap.add_argument("--ref-step-s", type=float, default=4.0)
+    ap.add_argument("--ref-step-s", type=float, default=4.0,
+                    help="reference arm: longest oracle sample per step")
+    ap.add_argument("--ref-budget-s", type=float, default=90.0,
+                    help="reference arm: oracle seconds for the whole run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fp8-pv", default="e4m3", choices=["e4m3", "f16"],
                     help="fp8 operands: precision of the P V product")

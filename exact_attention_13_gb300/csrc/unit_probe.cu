@@ -384,6 +384,182 @@ int run_mma_mode(const char* name, int nsm, double flop_per_mma) {
 }
 
 
+// The attention order with each product issued as one asm block (mma_chain_*_off, the form the
+// kernels use), one tcgen05.commit per product.  MODE 0: nothing else; 1: per product also a
+// try_wait on a completed barrier, a tcgen05 fence, a second commit and a clock store (the
+// issuing thread's bookkeeping); 2: warps 4-11 run independent FMA/ex2 work meanwhile (busy
+// softmax-like warps on every SMSP); 3: warps 4-11 move S, P and O through TMEM at the
+// softmax's pace.
+template <int MODE>
+__global__ void __launch_bounds__(384, 1) k_chain(long long* cyc, int nmma, int* err, float* sink) {
+  extern __shared__ __align__(1024) uint8_t smraw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  __shared__ uint64_t bar, done_bar;
+  __shared__ uint64_t dummy[4];
+  __shared__ uint32_t tbase;
+  __shared__ volatile int done;
+  const int tid = threadIdx.x;
+  for (int i = tid; i < 98304 / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(sm)[i] = 0x3C003C00u;
+  if (tid == 0) done = 0;
+  if (tid < 32) { tmem_alloc(smem_u32(&tbase), 512); tmem_relinquish(); }
+  if (tid == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    mbar_init(smem_u32(&done_bar), 1);
+    for (int q = 0; q < 4; ++q) mbar_init(smem_u32(&dummy[q]), 1);
+    fence_mbar_init();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before(); __syncthreads(); tc_fence_after();
+  const uint32_t tm = tbase;
+  if (tid == 0) {
+    mbar_arrive(smem_u32(&done_bar));  // phase 0 complete: the MODE 1 try_wait always succeeds
+    const uint32_t idS = instr_desc(128, 128, 1, false, false);
+    const uint32_t idPV = instr_desc(128, 128, 1, false, true);
+    const uint64_t da = smem_desc(smem_u32(sm), 16, 1024, kSwizzle128B);
+    const uint64_t db = smem_desc(smem_u32(sm + 32768), 16, 1024, kSwizzle128B);
+    const uint64_t dv = smem_desc(smem_u32(sm + 65536), 16384, 1024, kSwizzle128B);
+    const long long t0 = clock64();
+    for (int i = 0; i < nmma; i += 8) {
+      const int g = (i >> 3) & 3, h = g >> 1;
+      if (MODE == 1) {
+        if (!mbar_try_wait(smem_u32(&done_bar), 0)) atomicExch(err, 5);
+        tc_fence_after();
+      }
+      if ((g & 1) == 0)
+        mma_chain_ts_off<8, 0, 128, 8, 16, 24, 32, 40, 48, 56>(tm + 256 + h * 128, idPV, 1u,
+                                                              tm + h * 128, dv);
+      else
+        mma_chain_ss_off<8, 0, 2, 4, 6, 1024, 1026, 1028, 1030>(tm + h * 128, idS, 0u, da, db);
+      tc_commit(smem_u32(&dummy[g]));
+      if (MODE == 1) {
+        tc_commit(smem_u32(&dummy[(g + 1) & 3]));
+        reinterpret_cast<long long*>(sink)[(i >> 3) & 63] = clock64();
+      }
+    }
+    tc_commit(smem_u32(&bar));
+    int spins = 0;
+    while (!mbar_try_wait(smem_u32(&bar), 0)) { if (++spins > (1 << 26)) { atomicExch(err, 3); break; } }
+    cyc[blockIdx.x] = clock64() - t0;
+    done = 1;
+  } else if (tid >= 128 && MODE == 2) {
+    float a[8];
+    for (int k = 0; k < 8; ++k) a[k] = tid + k;
+    for (int it = 0; it < (1 << 20) && !done; ++it) {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          a[q] = (q == 4 || q == 7) ? ex2_mufu(a[q] * -1e-3f) : fmaf(a[q], 0.999f, 0.5f);
+      }
+    }
+    float t = 0.f;
+    for (int k = 0; k < 8; ++k) t += a[k];
+    if (t == 12345.f) sink[tid] = t;
+  } else if (tid >= 128 && MODE == 3) {
+    const int w = (tid / 32) % 4, h = (tid / 128) - 1;
+    const uint32_t sb = tm + (static_cast<uint32_t>(w * 32) << 16) + h * 128, ob = sb + 256;
+    float acc = tid * 1e-3f;
+    for (int it = 0; it < (1 << 16) && !done; ++it) {
+      uint32_t r[4][32];
+      for (int c = 0; c < 4; ++c) tmem_ld32(sb + c * 32, r[c]);
+      tmem_ld_wait();
+      float a2[8];
+      for (int k = 0; k < 8; ++k) a2[k] = __uint_as_float(r[0][k] & 0x3FFFFFFFu) * 1e-9f + acc;
+#pragma unroll 4
+      for (int k = 0; k < 64; ++k)
+        for (int q = 0; q < 8; ++q) a2[q] = fmaf(ex2_mufu(a2[q] * -1e-3f), 1e-3f, a2[q]);
+      for (int q = 0; q < 8; ++q) acc += a2[q];
+      uint32_t o[32];
+      for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(acc + k);
+      tmem_st32(sb, o);
+      tmem_st32(sb + 32, o);
+      tmem_st_wait();
+      if (it & 1) {
+        for (int c = 0; c < 4; ++c) {
+          uint32_t x[32];
+          tmem_ld32(ob + c * 32, x);
+          tmem_ld_wait();
+          for (int k = 0; k < 32; ++k) x[k] = __float_as_uint(__uint_as_float(x[k]) * 0.999f);
+          tmem_st32(ob + c * 32, x);
+        }
+        tmem_st_wait();
+      }
+    }
+    if (acc == 12345.f) sink[tid] = acc;
+  }
+  tc_fence_before(); __syncthreads(); tc_fence_after();
+  if (tid < 32) tmem_dealloc(tm, 512);
+}
+
+template <int MODE>
+void run_chain_mode(const char* name, int nsm) {
+  long long* cyc; int* err; float* sink;
+  CK(cudaMalloc(&cyc, nsm * 8)); CK(cudaMalloc(&err, 4)); CK(cudaMemset(err, 0, 4));
+  CK(cudaMalloc(&sink, 384 * 4)); CK(cudaMemset(sink, 0, 384 * 4));
+  CK(cudaFuncSetAttribute(k_chain<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, 120 * 1024));
+  const int nmma = 4096;
+  for (int rep = 0; rep < 2; ++rep) {
+    k_chain<MODE><<<nsm, 384, 120 * 1024>>>(cyc, nmma, err, sink);
+    CK(cudaGetLastError()); CK(cudaDeviceSynchronize());
+  }
+  std::vector<long long> c(nsm); CK(cudaMemcpy(c.data(), cyc, nsm * 8, cudaMemcpyDeviceToHost));
+  int herr; CK(cudaMemcpy(&herr, err, 4, cudaMemcpyDeviceToHost));
+  double mean = 0; for (auto v : c) mean += v; mean /= nsm;
+  printf("%-34s %7.1f cycles/mma  err=%d\n", name, mean / nmma, herr);
+  cudaFree(cyc); cudaFree(err); cudaFree(sink);
+}
+
+// mbarrier hand-off latency: warp 4 arrives at a recorded clock, thread 0 polls with try_wait
+// (MODE 0) or test_wait (MODE 1) and records when it sees the phase complete.
+template <int MODE>
+__global__ void __launch_bounds__(256, 1) k_wake(long long* out, int* err) {
+  __shared__ uint64_t bar;
+  __shared__ long long t_arr;
+  const int tid = threadIdx.x;
+  if (tid == 0) { mbar_init(smem_u32(&bar), 1); fence_mbar_init(); }
+  __syncthreads();
+  long long sum = 0;
+  for (int it = 0; it < 64; ++it) {
+    if (tid == 128) {
+      const long long s0 = clock64();
+      while (clock64() - s0 < 2000) {}
+      t_arr = clock64();
+      mbar_arrive(smem_u32(&bar));
+    } else if (tid == 0) {
+      int spins = 0;
+      for (;;) {
+        uint32_t ok;
+        if (MODE == 0) {
+          ok = mbar_try_wait(smem_u32(&bar), it & 1);
+        } else {
+          asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                       "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(ok) : "r"(smem_u32(&bar)), "r"(it & 1) : "memory");
+        }
+        if (ok) break;
+        if (++spins > (1 << 26)) { atomicExch(err, 1); break; }
+      }
+      sum += clock64();
+    }
+    __syncthreads();
+    if (tid == 0) sum -= t_arr;
+    __syncthreads();
+  }
+  if (tid == 0) out[blockIdx.x] = sum / 64;
+}
+
+template <int MODE>
+void run_wake(const char* name, int nsm) {
+  long long* out; int* err;
+  CK(cudaMalloc(&out, nsm * 8)); CK(cudaMalloc(&err, 4)); CK(cudaMemset(err, 0, 4));
+  k_wake<MODE><<<nsm, 256>>>(out, err); CK(cudaGetLastError()); CK(cudaDeviceSynchronize());
+  std::vector<long long> c(nsm); CK(cudaMemcpy(c.data(), out, nsm * 8, cudaMemcpyDeviceToHost));
+  int herr; CK(cudaMemcpy(&herr, err, 4, cudaMemcpyDeviceToHost));
+  double mean = 0; for (auto v : c) mean += v; mean /= nsm;
+  printf("%-34s %7.1f cycles arrive -> seen  err=%d\n", name, mean, herr);
+  cudaFree(out); cudaFree(err);
+}
+
+
 int main() {
   cudaDeviceProp prop; CK(cudaGetDeviceProperties(&prop, 0));
   printf("device %s  SMs %d  cc %d.%d  smem/block optin %zu  L2 %d\n", prop.name, prop.multiProcessorCount, prop.major, prop.minor,
@@ -411,6 +587,12 @@ int main() {
   run_mma_mode<35>("attention order + 1 commit/32", nsm, f128);
   run_mma_mode<33>("attention order + commit/group", nsm, f128);
   run_mma_mode<30>("attention order + TMEM ld/st", nsm, f128);
+  run_chain_mode<0>("chains: attention order + commit", nsm);
+  run_chain_mode<1>("chains + issuer bookkeeping", nsm);
+  run_chain_mode<2>("chains + busy warps on every SMSP", nsm);
+  run_chain_mode<3>("chains + softmax-paced TMEM S/P/O", nsm);
+  run_wake<0>("mbarrier hand-off, try_wait", nsm);
+  run_wake<1>("mbarrier hand-off, test_wait", nsm);
   printf("PROBE %s\n", ok ? "PASS" : "FAIL");
   return 0;
 }

@@ -28,3 +28,7 @@ def test_unit_probe(tmp_path):
     assert m and float(m.group(1)) >= 15.5
     m = re.search(r"mma SS bf16 M128 N128 K16\s+([\d.]+) cycles/mma", out)
     assert m and float(m.group(1)) < 70
+    # the attention order issued one product per asm block, as the kernels issue it, keeps the
+    # tensor core at its full rate
+    m = re.search(r"chains: attention order \+ commit\s+([\d.]+) cycles/mma\s+err=0", out)
+    assert m and float(m.group(1)) < 70
