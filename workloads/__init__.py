@@ -54,6 +54,17 @@ class Workload:
     def rows(self) -> int:
         return self.B * self.H * self.N
 
+    def score_matrix_bytes(self, elem_bytes: int) -> int:
+        """Bytes of one materialised N x N score (or probability) matrix per head: what the
+        fused path never writes."""
+        return self.N * self.N * elem_bytes
+
+    def io_bytes(self, out_elem_bytes: int = 2) -> int:
+        """HBM bytes the fused forward must move: Q, K, V read once, O and the fp32 LSE written
+        once."""
+        elem = 1 if self.dtype == "e4m3" else 2
+        return self.rows * self.d * (3 * elem + out_elem_bytes) + 4 * self.rows
+
     def describe(self) -> str:
         mask = "causal" if self.causal else "non-causal"
         qm = f" Q*{self.q_mult:g}" if self.q_mult != 1.0 else ""
