@@ -169,10 +169,13 @@ __device__ __forceinline__ void mma_acc(uint32_t tmem_d, uint32_t tmem_a, uint32
 template <bool PER_COLUMN, bool STORE, bool MASKED, typename VisFn>
 __device__ __forceinline__ void softmax_p(uint32_t t_s, float c, const float* l2, float l2_row,
                                           VisFn visible, float (&p)[64]) {
+  // pass 1's TMEM load is issued before pass 0's arithmetic, so its latency overlaps it
+  uint32_t rs[2][32];
+  tmem_ld32(t_s, rs[0]);
+  tmem_ld_wait();
+  tmem_ld32(t_s + 32, rs[1]);
 #pragma unroll
   for (int pass = 0; pass < 2; ++pass) {
-    uint32_t rs[32];
-    tmem_ld32(t_s + 32 * pass, rs);
     float lv[32];
     if constexpr (PER_COLUMN) {
       const float4* l4 = reinterpret_cast<const float4*>(l2 + 32 * pass);
@@ -188,13 +191,13 @@ __device__ __forceinline__ void softmax_p(uint32_t t_s, float c, const float* l2
 #pragma unroll
       for (int i = 0; i < 32; ++i) lv[i] = l2_row;
     }
-    tmem_ld_wait();
+    if (pass == 1) tmem_ld_wait();
     const uint64_t c2 = f32x2(c, c);
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
       // s c - LSE log2(e) for two columns in one packed fma
-      const uint64_t x2 = fma_f32x2(f32x2(__uint_as_float(rs[i]), __uint_as_float(rs[i + 1])), c2,
-                                    f32x2(-lv[i], -lv[i + 1]));
+      const uint64_t x2 = fma_f32x2(f32x2(__uint_as_float(rs[pass][i]), __uint_as_float(rs[pass][i + 1])),
+                                    c2, f32x2(-lv[i], -lv[i + 1]));
       float x0 = ex2_mufu(f32x2_lo(x2)), x1 = ex2_mufu(f32x2_hi(x2));
       if constexpr (MASKED) {
         x0 = visible(32 * pass + i) ? x0 : 0.f;
@@ -216,10 +219,12 @@ __device__ __forceinline__ void softmax_p(uint32_t t_s, float c, const float* l2
 template <bool PER_COLUMN>
 __device__ __forceinline__ void softmax_ds(uint32_t t_dp, const float* dl, float dl_row,
                                            const float (&p)[64]) {
+  uint32_t rd[2][32];
+  tmem_ld32(t_dp, rd[0]);
+  tmem_ld_wait();
+  tmem_ld32(t_dp + 32, rd[1]);
 #pragma unroll
   for (int pass = 0; pass < 2; ++pass) {
-    uint32_t rd[32];
-    tmem_ld32(t_dp + 32 * pass, rd);
     float dv[32];
     if constexpr (PER_COLUMN) {
       const float4* d4 = reinterpret_cast<const float4*>(dl + 32 * pass);
@@ -235,13 +240,13 @@ __device__ __forceinline__ void softmax_ds(uint32_t t_dp, const float* dl, float
 #pragma unroll
       for (int i = 0; i < 32; ++i) dv[i] = dl_row;
     }
-    tmem_ld_wait();
+    if (pass == 1) tmem_ld_wait();
     uint32_t pd[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int q = 32 * pass + 2 * i;
       // dS = P (dP - D), two columns per packed add and multiply
-      const uint64_t t2 = add_f32x2(f32x2(__uint_as_float(rd[2 * i]), __uint_as_float(rd[2 * i + 1])),
+      const uint64_t t2 = add_f32x2(f32x2(__uint_as_float(rd[pass][2 * i]), __uint_as_float(rd[pass][2 * i + 1])),
                                     f32x2(-dv[2 * i], -dv[2 * i + 1]));
       const uint64_t d2 = mul_f32x2(f32x2(p[q], p[q + 1]), t2);
       pd[i] = pack_bf16x2(f32x2_lo(d2), f32x2_hi(d2));
