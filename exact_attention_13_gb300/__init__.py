@@ -185,7 +185,8 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, descale=None,
     """Attention forward on torch CUDA tensors [B, H, N, d]; returns (o bf16, lse fp32).
 
     ``descale`` = (dq, dk, dv) for float8_e4m3fn operands; both of their products are fp8
-    unless ``pv16`` asks for an f16 P V product (P rounded to f16: slower, more accurate).  ``out``/``lse`` may be given
+    unless ``pv16`` asks for an f16 P V product (P rounded to f16: slower, more accurate); with
+    ``causal`` the first 256 query rows of each head always take the f16 P V product.  ``out``/``lse`` may be given
     (contiguous, right shape and dtype) to avoid allocation.  ``status`` is an optional int32
     CUDA tensor of one element the kernel sets to FA_ERR_DEVICE_TIMEOUT if a wait runs out.
     ``num_splits`` > 1 splits each query tile's keys over that many CTAs and merges the partial

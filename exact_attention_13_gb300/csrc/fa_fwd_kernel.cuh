@@ -9,7 +9,8 @@
 // slower on GB300, see the rescale note below):
 //
 //   warps 0-3  softmax, Q tile 0     one thread per query row: reads its S row from TMEM,
-//   warps 4-7  softmax, Q tile 1     updates (m, l), rescales its O row when m grew, writes the
+//   warps 4-7  softmax, Q tile 1     updates (m, l), rescales its O row when m grew (bf16: by more
+//                                    than the lazy threshold), writes the
 //                                    bf16/f16/e4m3 probabilities back into the S columns, and at the
 //                                    end normalises O, stores it and the row's log-sum-exp
 //   warp  8    TMA producer          Q tiles once, then K_j, V_j into the ring (full/empty
@@ -38,6 +39,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cstdint>
 
 #include "sm103_ptx.cuh"
@@ -82,20 +84,66 @@ constexpr uint64_t kWaitLimitNs = EXATTN_WAIT_LIMIT_NS;  // per wait (4 s in the
 #define EXATTN_INJECT_STALL 0
 #endif
 constexpr float kLn2 = 0.6931471805599453f;
-// Rescale threshold (log2 units).  0 rescales whenever a row's max grows; a positive value is the
-// lazy rescale of "FlashAttention4 精读", section 3.1.4 (the page uses 8, a factor 2^8), which
-// keeps a stale max and lets probabilities reach 2^threshold.  Exact in real arithmetic, but P
-// values above 1 are not exact in bf16/e4m3, so the dominant probability of a peaked row picks
-// up a rounding error (2^-9 relative in bf16) that the threshold-0 schedule avoids (there the
-// row max maps to exactly 1).  On logits spread over +-100 that costs up to ~0.009 in O, enough
-// to cross the 1e-2 gate, so the kernel uses 0.  The softmax warps rescale O themselves: a
-// separate correction warpgroup (16 warps; the softmax posts alpha, four warps rescale O while
-// the exponentials run) measured 9-16 % slower on GB300, because the 512-thread register split
-// leaves the softmax 168 registers and the alpha -> O-ready hand-off lands on the MMA's path.
-#ifndef EXATTN_RESCALE_LOG2
-#define EXATTN_RESCALE_LOG2 0.0f
+// Fraction of exponentials evaluated by the FMA polynomial instead of MUFU: one column in every
+// EXATTN_EMU_EVERY of an unmasked block (0 = MUFU only).  On GB300 MUFU does 32 ex2/clk/SM and
+// the softmax is issue-bound, so emulation costs time (1-in-8 measured -5..-7 %); off by default.
+#ifndef EXATTN_EMU_EVERY
+#define EXATTN_EMU_EVERY 0
 #endif
-constexpr float kRescaleLog2 = EXATTN_RESCALE_LOG2;
+
+// Format of the probabilities P handed to the P V product.
+enum class PFmt { kBf16, kF16, kE4m3 };
+
+template <bool FP8, bool PV16>
+__host__ __device__ constexpr PFmt p_fmt() {
+  return !FP8 ? PFmt::kBf16 : (PV16 ? PFmt::kF16 : PFmt::kE4m3);
+}
+
+// e4m3 probabilities are stored as 2^8 * p: the largest is 256 (< 448, the format's largest
+// finite value) and p down to 2^-14 stays out of the subnormal range.  O and l carry the same
+// factor, so it cancels in O / l; the LSE takes it back out.  bf16 and f16 P need no offset.
+template <PFmt PF>
+__host__ __device__ constexpr float p_offset_log2() {
+  return PF == PFmt::kE4m3 ? 8.f : 0.f;
+}
+
+// Lazy rescale ("FlashAttention4 精读", section 3.1.4): a row's O and l are rescaled only when
+// some row of the warp grew its max by more than this threshold (log2 units); otherwise the
+// stale max stays and probabilities may reach 2^threshold.  bf16 P takes the page's 8
+// (p <= 256).  fp8 operands take 0 (rescale whenever the max grows): for e4m3 P, whose offset is
+// already 2^8, a larger threshold would push the largest probabilities past e4m3's 448; the f16
+// P instances run out of registers with the extra bookkeeping (ptxas: spills in the block-scaled
+// instances).  Builds with the FMA exponential (EXATTN_EMU_EVERY > 0) take 0 as well: the
+// normaliser correction below recomputes a block's largest probability with MUFU, which matches
+// the loop's value only where the loop used MUFU for that column (at threshold 0 the row max is
+// 2^0 = 1 exactly on both units).  The softmax warps rescale O themselves: a separate correction
+// warpgroup (16 warps; the softmax posts alpha, four warps rescale O while the exponentials run)
+// measured 9-16 % slower on GB300, because the 512-thread register split leaves the softmax 168
+// registers and the alpha -> O-ready hand-off lands on the MMA's path.  EXATTN_RESCALE_LOG2
+// overrides the bf16 threshold (test builds).
+template <PFmt PF>
+__host__ __device__ constexpr float rescale_log2() {
+#if defined(EXATTN_RESCALE_LOG2)
+  return PF == PFmt::kBf16 && EXATTN_EMU_EVERY == 0 ? EXATTN_RESCALE_LOG2 : 0.f;
+#else
+  return PF == PFmt::kBf16 && EXATTN_EMU_EVERY == 0 ? 8.f : 0.f;
+#endif
+}
+
+// p rounded to P's format, as the conversions that write P round it (nearest even; e4m3
+// saturating), back in fp32.
+template <PFmt PF>
+__device__ __forceinline__ float round_p(float p) {
+  if constexpr (PF == PFmt::kBf16) {
+    return __uint_as_float(pack_bf16x2(p, 0.f) << 16);
+  } else if constexpr (PF == PFmt::kF16) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(pack_f16x2(p, 0.f) & 0xFFFFu)));
+  } else {
+    const uint32_t h = e4m3x2_to_f16x2(static_cast<uint16_t>(pack_e4m3x4(p, 0.f, 0.f, 0.f) & 0xFFFFu));
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu)));
+  }
+}
+
 // Design knobs (compile-time).  The defaults are the measured best on GB300 (A/B over whole
 // launches of the headline shapes): bf16 is MMA-issue-bound and prefers P published in one
 // part with a short L2 prefetch; e4m3 is softmax-bound and gains from PV starting on the first
@@ -114,12 +162,6 @@ __host__ __device__ constexpr int l2_prefetch_blocks() {
   return FP8 ? 6 : 2;
 #endif
 }
-// Fraction of exponentials evaluated by the FMA polynomial instead of MUFU: one column in every
-// EXATTN_EMU_EVERY of an unmasked block (0 = MUFU only).  On GB300 MUFU does 32 ex2/clk/SM and
-// the softmax is issue-bound, so emulation costs time (1-in-8 measured -5..-7 %); off by default.
-#ifndef EXATTN_EMU_EVERY
-#define EXATTN_EMU_EVERY 0
-#endif
 template <bool FP8>
 __host__ __device__ constexpr int p_parts() {
 #ifdef EXATTN_P_HALVES
@@ -137,6 +179,7 @@ struct KernelArgs {
   int* status;        // device status word (never null when launched by the library)
   int n;              // keys = queries per head
   int bh;             // batch * heads
+  int mblock0;        // first 256-row query block of this launch (launches may cover a range)
   float c;            // scale * log2(e) * descale_q * descale_k
   float out_mult;     // descale_v (1 for bf16)
   // fp8 block scaling (null for per-tensor descales): one fp32 descale per 128-row block of
@@ -146,14 +189,6 @@ struct KernelArgs {
   const float* dv_blk;
   int nblk;
 };
-
-// e4m3 probabilities are stored as 2^kPOffsetLog2 * p: the largest is 256 (< 448, the format's
-// largest finite value) and p down to 2^-14 stays out of the subnormal range.  O and l carry
-// the same factor, so it cancels in O / l; the LSE takes it back out.
-template <bool FP8>
-__host__ __device__ constexpr float p_offset_log2() {
-  return FP8 ? 8.f : 0.f;
-}
 
 // Compile-time geometry of one instance.  PV16 (fp8 operands only): the P V product runs in
 // f16 -- P rounded to f16 instead of e4m3, V widened from e4m3 to f16 in shared memory by a
@@ -252,8 +287,6 @@ __device__ __forceinline__ int kv_blocks_for_tile(int row0, int n) {
 // to bf16 (or e4m3) and written over the S columns in TMEM in two halves of 64 keys; after the
 // last half (or after each half when P_PARTS == 2) the warp publishes on the P barrier.  Returns
 // the fp32 sum of the unrounded p.
-enum class PFmt { kBf16, kF16, kE4m3 };
-
 template <bool MASKED, PFmt PF, int P_PARTS, int EMU_EVERY>
 __device__ __forceinline__ float exp_and_publish(float (&s)[128], float c, float m, int lim,
                                                  uint32_t t_s, uint32_t bar0, uint32_t bar1,
@@ -324,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const KernelArgs args) {
   using G = Geo<D, FP8, PV16>;
-  constexpr PFmt kPFmt = !FP8 ? PFmt::kBf16 : (PV16 ? PFmt::kF16 : PFmt::kE4m3);
+  constexpr PFmt kPFmt = p_fmt<FP8, PV16>();
   constexpr int kPHalves = p_parts<FP8>();
   constexpr int kL2PrefetchBlocks = l2_prefetch_blocks<FP8>();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -344,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // query blocks run from the last (heaviest: it sees every key block) to the first (y), i.e.
   // longest-processing-time-first over the whole grid ("FlashAttention4 精读", section 3.3).
   const int bh = CAUSAL ? blockIdx.x : blockIdx.y;
-  const int mblock = CAUSAL ? (gridDim.y - 1 - blockIdx.y) : blockIdx.x;
+  const int mblock = args.mblock0 + (CAUSAL ? (gridDim.y - 1 - blockIdx.y) : blockIdx.x);
   const int row0 = mblock * kCtaRows;
   const int nkv0_all = kv_blocks_for_tile<CAUSAL>(row0, n);
   const int nkv1_all = kv_blocks_for_tile<CAUSAL>(row0 + kTileRows, n);
@@ -622,6 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float c = args.c;
     float m_run = -INFINITY;  // running max of scaled logits, log2 units
     float l_run = 0.f;        // running sum of 2^(x - m_run) (times 2^p_offset_log2)
+    float l_fix = 0.f;        // sum over blocks of (rounded - unrounded) largest probability
     bool ok = true;
     // fp8 block scaling ("FlashAttention · InkStack", section 3.3.1 "Block Quantization"): the
     // score block (i, j) is scaled by dq_i dk_j, folded into the exponent's multiplier; the value
@@ -643,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     for (int j = 0; j < nkv_h; ++j) {
       float c_j = c;                             // multiplier of this key block's raw scores
-      float bias_j = p_offset_log2<FP8>();       // added to every exponent of the block
+      float bias_j = p_offset_log2<kPFmt>();     // added to every exponent of the block
       float l_mult = 1.f;                        // l gathers rowsum * l_mult
       if (blockscaled) {
         const float dk = __ldg(args.dk_blk + blk_base + jb + j);
@@ -713,12 +747,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_cand = fmaxf(m_run, mp[0] * c_j);
       if (threadIdx.x % 128 == 0) EXATTN_TRACE_EVENT(1, h, j);
 
-      // Rescale O and l when some row of the warp grew its max by more than kRescaleLog2 (the
-      // decision is warp-uniform because tcgen05.ld/st are warp-collective; rows whose max did
-      // not move get alpha = 1).
+      // Rescale O and l when some row of the warp grew its max by more than the lazy threshold
+      // (the decision is warp-uniform because tcgen05.ld/st are warp-collective; rows whose max
+      // did not move get alpha = 1).
       if (j == 0) {
         m_run = m_cand;
-      } else if (__any_sync(0xffffffffu, m_cand - m_run > kRescaleLog2)) {
+      } else if (__any_sync(0xffffffffu, m_cand - m_run > rescale_log2<kPFmt>())) {
         const float alpha = ex2_mufu(m_run - m_cand);
         uint32_t r[32];
 #pragma unroll
@@ -735,6 +769,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(t_o + cb * 32, r);
         }
         l_run *= alpha;
+        l_fix *= alpha;
         m_run = m_cand;
       }
       if (threadIdx.x % 128 == 0) EXATTN_TRACE_EVENT(10, h, j);
@@ -744,6 +779,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t pb0 = smem_u32(&ctl->p_full[h][0]);
       const uint32_t pb1 = smem_u32(&ctl->p_full[h][kPHalves == 2 ? 1 : 0]);
       const float m_shift = m_run - bias_j;
+      // The P V product sums the probabilities as rounded to P's format, l_run sums them
+      // unrounded.  Where a row's weight sits on one key, that key's rounding would reach O
+      // undiluted, and under the lazy rescale the largest probability is no longer exactly
+      // 2^0.  So O is divided by l_run plus, per block, the rounding of the block's largest
+      // probability (the same fma and ex2 as in the loop below give the same value), which
+      // makes O exact for a single dominant key; the LSE keeps l_run.  (Without the lazy
+      // rescale the row's largest probability is exactly 2^offset and needs no correction.)
+      if constexpr (rescale_log2<kPFmt>() > 0.f) {
+        const float p_top = ex2_mufu(fmaf(mp[0], c_j, -m_shift));
+        l_fix = fmaf(round_p<kPFmt>(p_top) - p_top, l_mult, l_fix);
+      }
       const float rowsum =
           masked ? exp_and_publish<true, kPFmt, kPHalves, 0>(s, c_j, m_shift, lim, t_s, pb0, pb1,
                                                              lane)
@@ -758,9 +804,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();
-        const float inv_l = (blockscaled ? dv_max : args.out_mult) / l_run;
+        const float inv_l = (blockscaled ? dv_max : args.out_mult) / (l_run + l_fix);
         const bool live = row < n;
-        const float lse_row = (m_run + lg2_mufu(l_run) - p_offset_log2<FP8>()) * kLn2;
+        const float lse_row = (m_run + lg2_mufu(l_run) - p_offset_log2<kPFmt>()) * kLn2;
         if (nsplit == 1) {
           __nv_bfloat16* orow = args.o + (static_cast<size_t>(bh) * n + (live ? row : 0)) * D;
 #pragma unroll

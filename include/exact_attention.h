@@ -50,7 +50,10 @@ typedef enum {
   FA_DTYPE_FP8_E4M3 = 1,      /* q, k, v are fp8 e4m3fn with fp32 descales; both products are
                                  fp8 ("FlashAttention · InkStack", section 3.3): P is rounded to
                                  e4m3, up to 2^-4 relative per probability, so a row whose mass
-                                 sits on a few keys carries that error on O */
+                                 sits on a few keys carries that error on O.  With the causal
+                                 mask the first 256 query rows of every head (which see at most
+                                 256 keys) take the f16 P V product of FP8_E4M3_PV16, in a
+                                 second, small launch on the same stream */
   FA_DTYPE_FP8_E4M3_PV16 = 2  /* as FP8_E4M3, but the P V product is f16: P rounded to f16, V
                                  widened exactly from e4m3 in shared memory (slower; S = Q K^T
                                  stays an fp8 product) */

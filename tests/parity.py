@@ -4,7 +4,9 @@ Tolerances (the targets of the method's accuracy statement): bf16 operands max|O
 and |LSE - LSE_ref| <= 1e-3; fp8-e4m3 operands 5e-2 and 5e-3.  O_ref is the exact fp64 result,
 while the kernel must round O to bf16, whose half-ulp alone is up to 2^-7 = 0.0078 for
 |O| in [2, 4) and 0.0156 for |O| in [4, 8).  Each element therefore gets the tolerance plus half
-a bf16 ulp of |O_ref|; the report also gives the error against bf16(O_ref).
+a bf16 ulp of |O_ref|.  The returned statistics also give the raw error against the unwidened
+tolerance: how many elements exceed it and the largest |O_ref| among them (where the kernel's
+bf16 output cannot get closer than the rounding of O_ref itself).
 """
 from __future__ import annotations
 
@@ -32,11 +34,14 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref, dtype: str, where: str = ""):
     err_o = np.abs(o - o_ref)
     err_l = np.abs(lse - lse_ref)
     ref_bf16 = torch.from_numpy(o_ref).to(torch.bfloat16).double().numpy()
+    over = err_o > tol_o
     stats = {
         "max_err_o": float(err_o.max()),
         "max_err_o_vs_bf16_ref": float(np.abs(o - ref_bf16).max()),
         "max_err_lse": float(err_l.max()),
         "mean_err_o": float(err_o.mean()),
+        "n_over_unwidened": int(over.sum()),
+        "max_abs_ref_over_unwidened": float(np.abs(o_ref[over]).max()) if over.any() else 0.0,
     }
     bad = err_o > tol_o + bf16_half_ulp(o_ref)
     if bad.any():
@@ -48,19 +53,3 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref, dtype: str, where: str = ""):
         raise AssertionError(f"{where}: LSE out of tolerance at {idx}: got {lse[idx]}, want "
                              f"{lse_ref[idx]} {stats}")
     return stats
-
-
-def compare_e4m3_p(o_gpu, lse_gpu, o_ref, lse_ref, vmax: float, where: str = ""):
-    """Bound for fp8 attention whose P V product is fp8 too, on rows that may put their mass on
-    a few keys (causal rows near the start): each probability is rounded to e4m3 (relative
-    error up to 2^-4), so |O - O_ref| <= 2^-4 max|V| plus the fp8 tolerance; the LSE is computed
-    from the unrounded probabilities and keeps the fp8 tolerance."""
-    tol_o, tol_l = TOL["e4m3"]
-    o = o_gpu.double().cpu().numpy()
-    lse = lse_gpu.double().cpu().numpy()
-    assert np.isfinite(o).all() and np.isfinite(lse).all(), where
-    err = np.abs(o - o_ref)
-    bound = 2.0 ** -4 * vmax + tol_o
-    assert err.max() <= bound, f"{where}: max |O - O_ref| {err.max()} > {bound}"
-    assert np.abs(lse - lse_ref).max() <= tol_l, f"{where}: LSE {np.abs(lse - lse_ref).max()}"
-    return {"max_err_o": float(err.max())}

@@ -4,7 +4,7 @@ The forward kernel supplies O and LSE (as a training step would); the oracle rec
 everything from Q, K, V and dO itself.  Tolerance (derived from the arithmetic): P and dS enter
 the tensor-core products rounded to bf16 (relative 2^-9 each), O enters D rounded to bf16, and
 the gradients are rounded to bf16 on output, so each element may be off by a few 2^-9 of the
-magnitude of its summands; the gate is |g - g_ref| <= 2e-2 max|g_ref| + half a bf16 ulp of
+magnitude of its summands; the gate is |g - g_ref| <= 1e-2 max|g_ref| + half a bf16 ulp of
 |g_ref| + a floor, per gradient tensor and head.  The floor covers gradients that vanish exactly
 (a row with one visible key has dS = 0): D_i is formed from the bf16-rounded O, so dP_ij - D_i
 carries up to 2^-8 sum_t |dO_it O_it| of rounding, which dQ multiplies by scale max|K| and dK by
@@ -25,7 +25,7 @@ from workloads import random_bwd_inputs
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda:0"
-REL = 2e-2
+REL = 1e-2
 
 
 @pytest.fixture(scope="module")

@@ -1,0 +1,106 @@
+"""Parity of the forward kernel's compile-time variants against the fp64 oracle.
+
+The library ships one schedule; two alternatives stay in the kernel source as compile-time knobs
+and are built here into libraries of their own, so that neither can rot unnoticed:
+
+* ``EXATTN_EMU_EVERY=2``: every second exponential of an unmasked key block is evaluated by the
+  FMA polynomial instead of MUFU (the partial emulation of "FlashAttention4 精读", section 3.1.3;
+  off in the library because GB300's MUFU does 32 ex2/clk/SM and the softmax is issue-bound).
+  Half of the columns is the heaviest use of the polynomial any setting makes.  (Such builds
+  rescale bf16 rows whenever the max grows: the lazy threshold needs every column on MUFU.)
+* ``EXATTN_RESCALE_LOG2=0``: the exact online-softmax schedule for bf16 P, O rescaled whenever
+  a row's max grows, instead of the lazy threshold of 8 of section 3.1.4.
+
+Each variant runs the small benchmark shape, the causal shape with Q scaled by 8 (logits over
+about +-100, the rescale stress case), a ragged causal head-dim-64 shape and two fp8 shapes, at
+the same tolerances as the library.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import shutil
+import subprocess
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = {
+    "emu2": ["-DEXATTN_EMU_EVERY=2"],
+    "rescale0": ["-DEXATTN_RESCALE_LOG2=0.0f"],
+}
+
+
+@pytest.fixture(scope="module", params=sorted(VARIANTS))
+def variant(request, tmp_path_factory):
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from exact_attention_13_gb300 import _build
+
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    lib_path = str(tmp_path_factory.mktemp(request.param) / f"libexattn_{request.param}.so")
+    flags = [f for f in _build.NVCC_FLAGS if f != "-lineinfo"]
+    subprocess.run([nvcc, *flags, *VARIANTS[request.param], "-o", lib_path, *_build.SOURCES],
+                   check=True)
+    lib = ctypes.CDLL(lib_path)
+    import exact_attention_13_gb300 as ea
+
+    res, args = ea.SIGNATURES["fa_fwd_ex"]
+    lib.fa_fwd_ex.restype, lib.fa_fwd_ex.argtypes = res, args
+    return request.param, lib
+
+
+def run_variant(lib, inp, causal, pv16=False):
+    import torch
+
+    import exact_attention_13_gb300 as ea
+
+    dev = torch.device("cuda:0")
+    q, k, v = (getattr(inp, n).to(dev) for n in "qkv")
+    B, H, N, d = q.shape
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    if inp.dtype == "bf16":
+        dtype = ea.FA_DTYPE_BF16
+    else:
+        dtype = ea.FA_DTYPE_FP8_E4M3_PV16 if pv16 else ea.FA_DTYPE_FP8_E4M3
+    opts = ea.FwdOpts(inp.descale_q, inp.descale_k, inp.descale_v, status.data_ptr())
+    rc = lib.fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B,
+                       H, N, d, 1.0 / math.sqrt(d), int(causal), dtype, ctypes.byref(opts),
+                       torch.cuda.current_stream(dev).cuda_stream)
+    assert rc == ea.FA_OK, rc
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return o, lse
+
+
+CASES = [
+    # (workload name or (B, H, N, d, dtype, causal, pv16))
+    "b1h1n256d64_bf16",
+    "b4h16n2048d128_bf16_causal_q8",
+    (1, 3, 1000, 64, "bf16", True, False),
+    (1, 2, 700, 128, "e4m3", False, False),
+    (1, 2, 1000, 64, "e4m3", True, True),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c if isinstance(c, str) else
+                                             "B{}H{}N{}d{}-{}-{}-{}".format(*c) for c in CASES])
+def test_variant_parity(variant, case):
+    from oracle import oracle
+    from tests.parity import compare
+    from workloads import WORKLOADS, make_inputs, random_inputs
+
+    name, lib = variant
+    if isinstance(case, str):
+        w = WORKLOADS[case]
+        inp, causal, pv16, dtype = make_inputs(w), w.causal, False, w.dtype
+    else:
+        B, H, N, d, dtype, causal, pv16 = case
+        inp = random_inputs(B, H, N, d, dtype, seed=N + 3 * d + int(causal))
+    o, lse = run_variant(lib, inp, causal, pv16)
+    o_ref, l_ref = oracle.attention_fwd_inputs(inp, 1.0 / math.sqrt(inp.q.shape[-1]), causal)
+    print(name, case, compare(o, lse, o_ref, l_ref, dtype, f"{name} {case}"))

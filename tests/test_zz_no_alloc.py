@@ -1,4 +1,4 @@
-"""The no-allocation key-split entry point (fa_fwd_split_noalloc) against the existing one.
+"""The no-allocation key-split entry point (fa_fwd_split_noalloc) against the existing one and the oracle.
 
 fa_fwd_split_noalloc serves callers that cannot allocate device memory when they call (a plug-in
 whose host owns the GPU's memory, a serving loop that must not stall on an allocation): its
@@ -18,16 +18,19 @@ def test_noalloc_matches_workspace_split_on_consecutive_calls():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     import exact_attention_13_gb300 as ea
+    from oracle import oracle
     from tests.parity import compare
     from workloads import random_inputs
 
     dev = torch.device("cuda:0")
     stream = torch.cuda.current_stream(dev).cuda_stream
-    # two calls in a row with different problems: the shared scratch keeps the first call's
-    # partials, which must not leak into the second call's result
-    cases = [(6001, True, 3, 1000, 128), (6002, False, 2, 777, 64)]
-    for seed, causal, splits, N, d in cases:
-        B, H = 1, 2
+    # calls in a row with different problems: the shared scratch keeps each call's partials, which
+    # must not leak into the next call's result -- a smaller problem after a larger one, then a
+    # larger one with more splits after a smaller one, so that stale partials sit where the new
+    # call reads
+    cases = [(6001, True, 3, 1, 2, 1000, 128), (6002, False, 2, 1, 2, 777, 64),
+             (6003, True, 4, 2, 4, 2000, 128)]
+    for seed, causal, splits, B, H, N, d in cases:
         inp = random_inputs(B, H, N, d, "bf16", seed=seed)
         q, k, v = (getattr(inp, n).to(dev) for n in "qkv")
         ref_o, ref_l = ea.fwd(q, k, v, causal=causal, num_splits=splits)  # caller workspace
@@ -38,8 +41,10 @@ def test_noalloc_matches_workspace_split_on_consecutive_calls():
                                      ea.FA_DTYPE_BF16, splits, stream=stream)
         assert rc == ea.FA_OK, rc
         torch.cuda.synchronize()
-        compare(o, lse, ref_o.double().cpu().numpy(), ref_l.double().cpu().numpy(), "bf16",
-                f"no-alloc split {splits} (seed {seed})")
+        # the same kernels on the same bytes with the same partials layout: bit-identical
+        assert torch.equal(o, ref_o) and torch.equal(lse, ref_l), (seed, splits)
+        o_ref, l_ref = oracle.attention_fwd_inputs(inp, 1.0 / math.sqrt(d), causal)
+        compare(o, lse, o_ref, l_ref, "bf16", f"no-alloc split {splits} (seed {seed})")
     assert ea.device_status(clear=True) == 0
 
 

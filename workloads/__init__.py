@@ -86,6 +86,11 @@ WORKLOADS = {
                                            "bf16", 1003, note="long sequence"),
     "b2h32n16384d128_e4m3": Workload("b2h32n16384d128_e4m3", 2, 32, 16384, 128, False, "e4m3",
                                      1004, note="fp8 operands, per-tensor descale"),
+    # not one of the method's benchmark shapes: the fp8 shape under the causal mask (its first
+    # query block of every head takes the f16 P V product)
+    "b2h32n16384d128_e4m3_causal": Workload("b2h32n16384d128_e4m3_causal", 2, 32, 16384, 128,
+                                            True, "e4m3", 1005,
+                                            note="fp8 operands, per-tensor descale, causal"),
     # not one of the method's benchmark shapes: a single long sequence with too few query blocks
     # to fill the GPU, where splitting the keys over CTAs (split-KV) pays
     "b1h1n16384d128_bf16": Workload("b1h1n16384d128_bf16", 1, 1, 16384, 128, False, "bf16", 1100,
