@@ -3,16 +3,19 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-One step is one attention forward (the whole hot path: one kernel launch) over one batch of
-seeded synthetic inputs already resident in HBM.  The default workload is the headline shape
+One step is one attention forward (the whole hot path: one kernel launch; two for causal fp8
+with an fp8 P V product, three with key splits) over one batch of seeded synthetic inputs
+already resident in HBM.  The default workload is the headline shape
 B=2, H=32, N=8192, d=128, bf16, non-causal; every input tensor (134 MB each, 403 MB for Q, K, V)
 is larger than the 129 MB L2, so consecutive steps do not find their inputs in L2.
 
 Prints ONE JSON line on rank 0: the metric (attention forward TFLOPS, 4·B·H·N²·d, halved for
 the causal mask), the device-timed value, an end-to-end value through the C ABI with host
 buffers (H2D of Q, K, V and D2H of O, LSE inside the timed region), the roofline of the kernel
-against the measured peak, SM clocks sampled during the timed region, and the fp64 CPU oracle
-timed on a bounded sample of the same workload.  ``--impl reference`` times that oracle as the
+against the measured peak, SM clocks read from NVML during the timed region, a sustained leg
+(the same step back to back for about two seconds, with its own clock record, against the
+sustained peak), and the fp64 CPU oracle timed on a bounded sample of the same workload, whose
+outputs also give the raw errors of the GPU result on that sample.  ``--impl reference`` times that oracle as the
 reference arm instead.  Under torchrun every rank runs its own copy of the workload (independent
 (batch, head) problems: weak scaling, no collective on the data path).
 """
@@ -35,7 +38,7 @@ from workloads import HEADLINE, WORKLOADS, make_inputs  # noqa: E402
 METRIC = "attention fwd TFLOPS and % of GB300 dense BF16/FP8 peak (1 GPU, device-timed)"
 UNIT = "TFLOPS"
 FP8_OVER_BF16 = 4.5 / 2.25          # nominal dense fp8 : bf16 tensor ratio
-EXP_PER_CLK_SM = 32                 # measured MUFU ex2 rate on this GB300 (probe)
+EXP_PER_CLK_SM = 32                 # MUFU ex2 results per clock per SM on GB300 (measured)
 
 
 def peaks():
@@ -46,6 +49,101 @@ def peaks():
         return {"bf16": float(p["bf16_tflops"]), "bf16_sustained": float(p["bf16_tflops_sustained"]),
                 "hbm_gbs": float(p["hbm_gbs"]), "source": "measured"}
     return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+class NvmlClocks:
+    """SM clock, power and clock-event reasons read in-process from NVML every ``period_s`` on a
+    background thread while the block runs (read-only queries: no clock, power or other GPU
+    setting is changed).  Falls back to ``nvidia-smi`` sampling where NVML cannot be loaded."""
+
+    REASON_BITS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x4: "sw_power_cap"}
+
+    def __init__(self, device, period_s: float = 0.002):
+        import ctypes
+        import threading
+
+        self.period = period_s
+        self.rows = []
+        self.fallback = None
+        self._stop = threading.Event()
+        self._thread = None
+        self.nvml = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            self.handle = ctypes.c_void_p()
+            import torch
+
+            props = torch.cuda.get_device_properties(device)
+            uuid = getattr(props, "uuid", None)
+            found = False
+            if uuid is not None:
+                found = nv.nvmlDeviceGetHandleByUUID(f"GPU-{uuid}".encode(),
+                                                     ctypes.byref(self.handle)) == 0
+            if not found:
+                found = nv.nvmlDeviceGetHandleByIndex_v2(device.index or 0,
+                                                         ctypes.byref(self.handle)) == 0
+            if not found:
+                raise OSError("no NVML handle")
+            self.nvml = nv
+            self._u = ctypes.c_uint()
+            self._ull = ctypes.c_ulonglong()
+            nv.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(self._u))
+            self.max_mhz = float(self._u.value)
+        except (OSError, AttributeError):
+            self.nvml = None
+            self.fallback = ClockSampler(device.index or 0)
+
+    def _sample(self):
+        import ctypes
+
+        nv, h = self.nvml, self.handle
+        while not self._stop.is_set():
+            mhz = pw = reasons = None
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(self._u)) == 0:
+                mhz = float(self._u.value)
+            if nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(self._u)) == 0:
+                pw = self._u.value / 1000.0
+            if nv.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(self._ull)) == 0:
+                reasons = int(self._ull.value)
+            if mhz is not None:
+                self.rows.append((mhz, pw, reasons))
+            self._stop.wait(self.period)
+
+    def __enter__(self):
+        import threading
+
+        if self.nvml is None:
+            self.fallback.__enter__()
+            return self
+        self.rows = []
+        self._stop.clear()
+        self._thread = threading.Thread(target=self._sample, daemon=True)
+        self._thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.nvml is None:
+            self.fallback.__exit__(*exc)
+            return
+        self._stop.set()
+        self._thread.join(timeout=5)
+
+    def summary(self):
+        if self.nvml is None:
+            return self.fallback.summary()
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no samples"],
+                    "source": "nvml"}
+        names = sorted({name for _, _, r in self.rows if r is not None
+                        for bit, name in self.REASON_BITS.items() if r & bit})
+        pws = [p for _, p, _ in self.rows if p is not None]
+        return {"sm_mhz": statistics.median(m for m, _, _ in self.rows),
+                "sm_max_mhz": self.max_mhz, "power_w_max": max(pws) if pws else None,
+                "samples": len(self.rows), "period_ms": 1e3 * self.period, "reasons": names,
+                "source": "nvml (in-process reads during the timed region)"}
 
 
 class ClockSampler:
@@ -104,13 +202,14 @@ class ClockSampler:
                 "power_w_max": pmax, "samples": len(loaded), "reasons": reasons}
 
 
-def oracle_sample_rate(inp, w, target_s: float, rerun=None):
+def oracle_sample_rate(inp, w, target_s: float, rerun=None, outputs=None):
     """Time the fp64 oracle on a sample of the workload sized for about target_s seconds.
 
     The sample is a set of query rows (spread over the sequence) of the first heads; the rate is
     the attention-forward flops of those rows (4 * keys * d each) per second, in TFLOPS.  With
     a list as `rerun`, a callable that runs the same sample again (returning TFLOPS, seconds) is
-    appended to it.
+    appended to it; with a dict as `outputs`, the oracle's O and LSE of the timed sample and the
+    sample's coordinates are stored in it.
     """
     from oracle import oracle
 
@@ -127,13 +226,17 @@ def oracle_sample_rate(inp, w, target_s: float, rerun=None):
                         inp.descale_q, inp.descale_k, inp.descale_v)
         rows = sorted(rows_all[:nrows])
         t0 = time.perf_counter()
-        orc.attention_fwd(sub.raw("q"), sub.raw("k"), sub.raw("v"), w.scale, w.causal, sub.dtype,
-                          (sub.descale_q, sub.descale_k, sub.descale_v), rows, cores)
+        o_ref, l_ref = orc.attention_fwd(sub.raw("q"), sub.raw("k"), sub.raw("v"), w.scale,
+                                         w.causal, sub.dtype,
+                                         (sub.descale_q, sub.descale_k, sub.descale_v), rows,
+                                         cores)
         dt = time.perf_counter() - t0
+        last.update(o=o_ref, lse=l_ref, nb=nb, heads=b_heads, rows=rows)
         keys = sum((r + 1) if w.causal else w.N for r in rows)
         nh = sub.q.shape[0] * sub.q.shape[1]
         return 4.0 * keys * w.d * nh / dt / 1e12, dt, nh, len(rows)
 
+    last = {}
     heads, nrows = min(bh, 2), min(len(rows_all), 256)
     tf, dt, nh, nr = run(heads, nrows)
     # grow rows first, then heads, to reach the target duration; shrink rows if one probe
@@ -151,7 +254,28 @@ def oracle_sample_rate(inp, w, target_s: float, rerun=None):
               f"({'causal' if w.causal else 'all'} keys each), fp64 on {cores} threads")
     if rerun is not None:
         rerun.append(lambda: run(heads, nrows)[:2])
+    if outputs is not None:
+        outputs.update(last)
     return tf, dt, cores, sample
+
+
+def sample_parity(o, lse, ref, dtype: str):
+    """Raw errors of the GPU output against the oracle on the CPU-baseline sample: max |O - O_ref|
+    and max |LSE - LSE_ref|, elements over the unwidened O tolerance (1e-2 bf16, 5e-2 fp8), and
+    elements over the tolerance widened by half a bf16 ulp of |O_ref| (the rounding of O)."""
+    import numpy as np
+
+    nb, nh, rows = ref["nb"], ref["heads"], ref["rows"]
+    og = o[:nb, :nh, rows].double().cpu().numpy()
+    lg = lse[:nb, :nh, rows].double().cpu().numpy()
+    tol_o, tol_l = (5e-2, 5e-3) if dtype == "e4m3" else (1e-2, 1e-3)
+    err = np.abs(og - ref["o"])
+    a = np.abs(ref["o"])
+    half_ulp = np.where(a > 0, np.exp2(np.floor(np.log2(np.where(a > 0, a, 1.0))) - 8), 0.0)
+    return {"rows": len(rows), "heads": nb * nh, "max_err_o": float(err.max()),
+            "max_err_lse": float(np.abs(lg - ref["lse"]).max()), "tol_o": tol_o, "tol_lse": tol_l,
+            "n_over_tol_o": int((err > tol_o).sum()),
+            "n_over_tol_o_plus_half_ulp": int((err > tol_o + half_ulp).sum())}
 
 
 KERNEL_SOURCES = ["exact_attention_13_gb300/csrc/fa_fwd_kernel.cuh",
@@ -248,6 +372,14 @@ def run_reference(args, w, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def launches_per_step(w, args, fp8_pv: bool) -> int:
+    """Kernel launches of one attention call: the forward kernel (twice for causal fp8 with an
+    fp8 P V product longer than one 256-row query block: its first block runs the f16 P V
+    instance), plus the merge kernel with key splits."""
+    fwd = 2 if (w.causal and fp8_pv and w.N > 256) else 1
+    return fwd + (1 if args.splits > 1 else 0)
+
+
 def run_ours(args, w, world, rank, local):
     import torch
 
@@ -308,15 +440,16 @@ def run_ours(args, w, world, rank, local):
 
     # ---- device-timed region: K launches back to back on one stream
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        barrier()
-        torch.cuda.synchronize()
+    clk = NvmlClocks(dev)
+    barrier()
+    torch.cuda.synchronize()
+    with clk:
         start.record(stream)
         for _ in range(args.steps):
             step()
         end.record(stream)
         torch.cuda.synchronize()
-        barrier()
+    barrier()
     ms = start.elapsed_time(end) / args.steps
     clocks = clk.summary()
     ms_max = max_over_ranks(ms, world, dev)
@@ -377,6 +510,29 @@ def run_ours(args, w, world, rank, local):
     torch.cuda.synchronize()
     e_ms = max_over_ranks(e_start.elapsed_time(e_end) / args.steps, world, dev)
     assert ea.device_status() == 0, "device wait timed out during the end-to-end run"
+    # ---- sustained: the device-timed step back to back for about --sustained-s seconds, with
+    # its own clock record (the timed region above is a burst of a few tens of milliseconds); run
+    # last, so that the power-capped clocks it settles at do not carry into the other legs
+    sustained = None
+    if args.sustained_s > 0:
+        n_sus = max(args.steps, int(math.ceil(args.sustained_s * 1e3 / ms)))
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sclk = NvmlClocks(dev, period_s=0.01)
+        barrier()
+        torch.cuda.synchronize()
+        with sclk:
+            s0.record(stream)
+            for _ in range(n_sus):
+                step()
+            s1.record(stream)
+            torch.cuda.synchronize()
+        barrier()
+        s_ms = max_over_ranks(s0.elapsed_time(s1) / n_sus, world, dev)
+        sustained = {"steps": n_sus, "seconds": n_sus * s_ms * 1e-3, "ms_per_step": s_ms,
+                     "value": job_tflops(w.flops, world, s_ms), "unit": UNIT,
+                     "clocks": sclk.summary()}
+        assert ea.device_status() == 0, "device wait timed out during the sustained run"
+
     h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh, *sh))
     d2h = oh[0].numel() * oh[0].element_size() + lh[0].numel() * lh[0].element_size()
 
@@ -391,11 +547,16 @@ def run_ours(args, w, world, rank, local):
     if is_fp8 and pv16:
         # half the flops (Q K^T) at the fp8 rate, half (P V) at the f16 rate: the time-weighted
         # peak is 1 / (0.5 / (2 P) + 0.5 / P) = 4 P / 3
-        peak = pk["bf16"] * 4.0 / 3.0
+        dtype_mult = 4.0 / 3.0
         peak_note = " x 4/3 (Q K^T fp8 at 2x, P V f16 at 1x)"
     else:
-        peak = pk["bf16"] * (FP8_OVER_BF16 if is_fp8 else 1.0)
+        dtype_mult = FP8_OVER_BF16 if is_fp8 else 1.0
         peak_note = " x 2 (nominal fp8:bf16)" if is_fp8 else ""
+    peak = pk["bf16"] * dtype_mult
+    if sustained is not None:
+        sustained["peak"] = pk["bf16_sustained"] * dtype_mult
+        sustained["frac"] = sustained["value"] / world / sustained["peak"]
+        sustained["peak_kind"] = f"{pk['source']} cuBLAS bf16 sustained" + peak_note
     achieved = flops_rank / (ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak,
@@ -430,12 +591,18 @@ def run_ours(args, w, world, rank, local):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
                 "pipelining": "2 buffer sets; H2D, kernel, D2H on 3 streams"},
-        "gpu_launches": args.steps * (2 if args.splits > 1 else 1),
+        "gpu_launches": args.steps * launches_per_step(w, args, is_fp8 and not pv16),
+        "sustained": sustained,
     }
     if not args.no_cpu_baseline:
-        tf, dt, cores, sample = oracle_sample_rate(inp, w, target_s=args.cpu_s)
+        ref = {}
+        tf, dt, cores, sample = oracle_sample_rate(inp, w, target_s=args.cpu_s, outputs=ref)
         line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": sample, "seconds": dt}
+        # the same sample compared with the GPU's output (block-scaled fp8 quantises other
+        # inputs on the GPU, so it has no per-tensor oracle sample here)
+        line["parity"] = (sample_parity(o, lse, ref, w.dtype) if not block else
+                          {"skipped": "block-scaled inputs differ from the oracle sample"})
     print(json.dumps(line), flush=True)
 
 
@@ -465,7 +632,7 @@ def run_quantize(args, w, world, rank, local):
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
+    with NvmlClocks(dev) as clk:
         if world > 1:
             import torch.distributed as dist
 
@@ -528,7 +695,7 @@ def run_backward(args, w, world, rank, local):
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
+    with NvmlClocks(dev) as clk:
         if world > 1:
             import torch.distributed as dist
 
@@ -577,6 +744,8 @@ def main():
     ap.add_argument("--ref-budget-s", type=float, default=90.0,
                     help="reference arm: oracle seconds for the whole run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sustained-s", type=float, default=2.0,
+                    help="seconds of the sustained leg (0 = off)")
     ap.add_argument("--fp8-pv", default="e4m3", choices=["e4m3", "f16"],
                     help="fp8 operands: precision of the P V product")
     ap.add_argument("--fp8-scaling", default="tensor", choices=["tensor", "block"],

@@ -70,6 +70,21 @@ constexpr int kTraceMaxJ = 512;
 #endif
 
 constexpr int kThreads = 384;
+// Warp roles: softmax warps 0-7, then the control warpgroup 8-11 (producer, MMA issuer, two V
+// converters).  With the control warpgroup in warps 0-3 instead, the headline shape measured
+// 2 % slower and the causal d128 shape 3 % slower (fp8 +1 %).
+constexpr int kCtlWarp0 = 8;
+constexpr int kProducerWarp = kCtlWarp0;
+constexpr int kMmaWarp = kCtlWarp0 + 1;
+constexpr int kConvWarp0 = kCtlWarp0 + 2;
+constexpr int kSoftmaxWarp0 = 0;
+// setmaxnreg split of the 384 x 168 launch registers: 128 x (2 kSoftmaxRegs + kCtlRegs)
+#ifndef EXATTN_SOFTMAX_REGS
+#define EXATTN_SOFTMAX_REGS 216
+#endif
+constexpr int kSoftmaxRegs = EXATTN_SOFTMAX_REGS;
+constexpr int kCtlRegs = (384 * 168 - 256 * kSoftmaxRegs) / 128;
+static_assert(kCtlRegs % 8 == 0 && kCtlRegs >= 24, "setmaxnreg takes multiples of 8");
 constexpr int kTileRows = 128;       // query rows per Q tile, keys per K/V block
 constexpr int kCtaRows = 2 * kTileRows;
 constexpr int kStatusTimeout = 5;    // FA_ERR_DEVICE_TIMEOUT
@@ -109,25 +124,27 @@ __host__ __device__ constexpr float p_offset_log2() {
 
 // Lazy rescale ("FlashAttention4 精读", section 3.1.4): a row's O and l are rescaled only when
 // some row of the warp grew its max by more than this threshold (log2 units); otherwise the
-// stale max stays and probabilities may reach 2^threshold.  bf16 P takes the page's 8
-// (p <= 256).  fp8 operands take 0 (rescale whenever the max grows): for e4m3 P, whose offset is
-// already 2^8, a larger threshold would push the largest probabilities past e4m3's 448; the f16
-// P instances run out of registers with the extra bookkeeping (ptxas: spills in the block-scaled
-// instances).  Builds with the FMA exponential (EXATTN_EMU_EVERY > 0) take 0 as well: the
-// normaliser correction below recomputes a block's largest probability with MUFU, which matches
-// the loop's value only where the loop used MUFU for that column (at threshold 0 the row max is
-// 2^0 = 1 exactly on both units).  The softmax warps rescale O themselves: a separate correction
-// warpgroup (16 warps; the softmax posts alpha, four warps rescale O while the exponentials run)
-// measured 9-16 % slower on GB300, because the 512-thread register split leaves the softmax 168
-// registers and the alpha -> O-ready hand-off lands on the MMA's path.  EXATTN_RESCALE_LOG2
-// overrides the bf16 threshold (test builds).
+// stale max stays and probabilities may reach 2^threshold.  bf16 and f16 P take the page's 8
+// (p <= 256).  e4m3 P, stored with the offset 2^8, takes 0.8: its largest probability stays
+// below 2^8.8 < 448, e4m3's largest finite value, and since a row's max mostly grows by less than
+// that once a few blocks are in, most rescales are still skipped.  Builds with the FMA
+// exponential (EXATTN_EMU_EVERY > 0) take 0: the normaliser correction below recomputes a
+// block's largest probability with MUFU, which matches the loop's value only where the loop used
+// MUFU for that column (at threshold 0 the row max is 2^offset exactly on both units).  The
+// softmax warps rescale O themselves: a separate correction warpgroup (16 warps; the softmax
+// posts alpha, four warps rescale O while the exponentials run) measured 9-16 % slower on GB300,
+// because the 512-thread register split leaves the softmax 168 registers and the alpha -> O-ready
+// hand-off lands on the MMA's path.  EXATTN_RESCALE_LOG2 overrides the bf16 threshold (test
+// builds).
 template <PFmt PF>
 __host__ __device__ constexpr float rescale_log2() {
 #if defined(EXATTN_RESCALE_LOG2)
-  return PF == PFmt::kBf16 && EXATTN_EMU_EVERY == 0 ? EXATTN_RESCALE_LOG2 : 0.f;
+  constexpr float kBf16 = EXATTN_RESCALE_LOG2;
 #else
-  return PF == PFmt::kBf16 && EXATTN_EMU_EVERY == 0 ? 8.f : 0.f;
+  constexpr float kBf16 = 8.f;
 #endif
+  return EXATTN_EMU_EVERY != 0 ? 0.f
+                               : (PF == PFmt::kBf16 ? kBf16 : (PF == PFmt::kF16 ? 8.f : 0.8f));
 }
 
 // p rounded to P's format, as the conversions that write P round it (nearest even; e4m3
@@ -392,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nkv_load = nkv0 > nkv1 ? nkv0 : nkv1;
 
   // ---------------------------------------------------------------- setup
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&ctl->tmem_base), 512);
     tmem_relinquish();
   }
@@ -422,9 +439,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // registers: the producer/MMA warpgroup gives most of its share to the softmax warpgroups
   // (384 threads x 168 at launch = 128 x (216 + 216 + 72))
-  if (warp >= 8) {
-    regs_dec<72>();
-  if (warp == 8) {
+  if (warp >= kCtlWarp0 && warp < kCtlWarp0 + 4) {
+    regs_dec<kCtlRegs>();
+  if (warp == kProducerWarp) {
     // ============================================================ TMA producer
     if (lane == 0) {
       tma_prefetch_map(&map_q);
@@ -487,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kMmaWarp) {
     // ============================================================ MMA issuer
     if (lane == 0 && nkv_load > 0) {
       bool ok = wait_phase(smem_u32(&ctl->q_full), 0, abort_flag, args.status);
@@ -596,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // stores.
       constexpr int kChunks = D / 16;            // 16-element chunks per row
       constexpr int kRowsPerPass = 32 / kChunks;
-      const int row_begin = (warp - 10) * (kTileRows / 2);
+      const int row_begin = (warp - kConvWarp0) * (kTileRows / 2);
       const int c = lane % kChunks;
       const int box_off = (c / 4) * (kTileRows * 128);
       const int cc = 2 * (c % 4);
@@ -641,9 +658,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   } else {
-    regs_inc<216>();
+    regs_inc<kSoftmaxRegs>();
     // ============================================================ softmax / epilogue
-    const int h = warp / 4;
+    const int h = (warp - kSoftmaxWarp0) / 4;
     const int w4 = warp % 4;
     const int nkv_h = h == 0 ? nkv0 : nkv1;
     const int nkv_h_all = h == 0 ? nkv0_all : nkv1_all;
@@ -863,7 +880,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---------------------------------------------------------------- teardown
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

@@ -27,12 +27,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-__device__ __forceinline__ uint32_t lane_id() {
-  uint32_t l;
-  asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));
-  return l;
-}
-
 // Register budget moves between warpgroups (all warps of a warpgroup execute the same one).
 template <int N>
 __device__ __forceinline__ void regs_inc() {
@@ -41,11 +35,6 @@ __device__ __forceinline__ void regs_inc() {
 template <int N>
 __device__ __forceinline__ void regs_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-
-// Named barrier among a subset of warps (id 1..15; id 0 is __syncthreads).
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ------------------------------------------------------------------------------------------
@@ -134,24 +123,6 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int32
                : "memory");
 }
 
-// 3-D tiled store shared -> global (rows outside the tensor are clipped by the map).
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t c0,
-                                             int32_t c1, int32_t c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::
-          "l"(reinterpret_cast<uint64_t>(map)),
-      "r"(src), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_store_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-__device__ __forceinline__ void tma_store_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 // ------------------------------------------------------------------------------------------
 // tcgen05: tensor memory
 // ------------------------------------------------------------------------------------------
@@ -226,190 +197,11 @@ __device__ __forceinline__ void mma_f8_ts(uint32_t d, uint32_t a_tmem, uint64_t 
       : "memory");
 }
 
-// ---- MMA chains: all MMAs of one product in a single asm block, descriptors precomputed.
-// Issued this way the tensor core runs the attention kernel's S / P V alternation at its full
-// rate (64 cycles per 128x128x16 bf16 MMA, measured); the same MMAs issued one asm statement at
-// a time ran at 92-113 cycles.  The first MMA accumulates into D when acc0 != 0, the others
-// always accumulate.  KIND: 0 = kind::f16, 1 = kind::f8f6f4.
-
-template <int KIND>
-__device__ __forceinline__ void mma_chain_ss2(uint32_t d, uint32_t idesc, uint32_t acc0,
-                                               const uint64_t (&a)[2], const uint64_t (&b)[2]) {
-  if constexpr (KIND == 0) {
-    asm volatile(
-      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %5, %1, p;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %6, %1, t;\n\t"
-      "}" ::"r"(d), "r"(idesc), "r"(acc0), "l"(a[0]), "l"(a[1]), "l"(b[0]), "l"(b[1])
-      : "memory");
-  } else {
-    asm volatile(
-      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, %5, %1, p;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %4, %6, %1, t;\n\t"
-      "}" ::"r"(d), "r"(idesc), "r"(acc0), "l"(a[0]), "l"(a[1]), "l"(b[0]), "l"(b[1])
-      : "memory");
-  }
-}
-
-template <int KIND>
-__device__ __forceinline__ void mma_chain_ss4(uint32_t d, uint32_t idesc, uint32_t acc0,
-                                               const uint64_t (&a)[4], const uint64_t (&b)[4]) {
-  if constexpr (KIND == 0) {
-    asm volatile(
-      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %1, p;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %9, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %10, %1, t;\n\t"
-      "}" ::"r"(d), "r"(idesc), "r"(acc0), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3])
-      : "memory");
-  } else {
-    asm volatile(
-      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, %7, %1, p;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %4, %8, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %5, %9, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %6, %10, %1, t;\n\t"
-      "}" ::"r"(d), "r"(idesc), "r"(acc0), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3])
-      : "memory");
-  }
-}
-
-template <int KIND>
-__device__ __forceinline__ void mma_chain_ss8(uint32_t d, uint32_t idesc, uint32_t acc0,
-                                               const uint64_t (&a)[8], const uint64_t (&b)[8]) {
-  if constexpr (KIND == 0) {
-    asm volatile(
-      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %1, p;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %17, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %10, %18, %1, t;\n\t"
-      "}" ::"r"(d), "r"(idesc), "r"(acc0), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7])
-      : "memory");
-  } else {
-    asm volatile(
-      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, %11, %1, p;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %4, %12, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %5, %13, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %6, %14, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %7, %15, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %8, %16, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %9, %17, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %10, %18, %1, t;\n\t"
-      "}" ::"r"(d), "r"(idesc), "r"(acc0), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7])
-      : "memory");
-  }
-}
-
-template <int KIND>
-__device__ __forceinline__ void mma_chain_ts2(uint32_t d, uint32_t idesc, uint32_t acc0,
-                                               const uint32_t (&a)[2], const uint64_t (&b)[2]) {
-  if constexpr (KIND == 0) {
-    asm volatile(
-      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %5, %1, p;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %6, %1, t;\n\t"
-      "}" ::"r"(d), "r"(idesc), "r"(acc0), "r"(a[0]), "r"(a[1]), "l"(b[0]), "l"(b[1])
-      : "memory");
-  } else {
-    asm volatile(
-      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%3], %5, %1, p;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%4], %6, %1, t;\n\t"
-      "}" ::"r"(d), "r"(idesc), "r"(acc0), "r"(a[0]), "r"(a[1]), "l"(b[0]), "l"(b[1])
-      : "memory");
-  }
-}
-
-template <int KIND>
-__device__ __forceinline__ void mma_chain_ts4(uint32_t d, uint32_t idesc, uint32_t acc0,
-                                               const uint32_t (&a)[4], const uint64_t (&b)[4]) {
-  if constexpr (KIND == 0) {
-    asm volatile(
-      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %7, %1, p;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %8, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %9, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %10, %1, t;\n\t"
-      "}" ::"r"(d), "r"(idesc), "r"(acc0), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3])
-      : "memory");
-  } else {
-    asm volatile(
-      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%3], %7, %1, p;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%4], %8, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%5], %9, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%6], %10, %1, t;\n\t"
-      "}" ::"r"(d), "r"(idesc), "r"(acc0), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3])
-      : "memory");
-  }
-}
-
-template <int KIND>
-__device__ __forceinline__ void mma_chain_ts8(uint32_t d, uint32_t idesc, uint32_t acc0,
-                                               const uint32_t (&a)[8], const uint64_t (&b)[8]) {
-  if constexpr (KIND == 0) {
-    asm volatile(
-      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %11, %1, p;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %12, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %13, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %14, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %15, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %16, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %17, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%10], %18, %1, t;\n\t"
-      "}" ::"r"(d), "r"(idesc), "r"(acc0), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7])
-      : "memory");
-  } else {
-    asm volatile(
-      "{\n\t.reg .pred p, t;\n\tsetp.ne.b32 p, %2, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%3], %11, %1, p;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%4], %12, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%5], %13, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%6], %14, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%7], %15, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%8], %16, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%9], %17, %1, t;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%10], %18, %1, t;\n\t"
-      "}" ::"r"(d), "r"(idesc), "r"(acc0), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7])
-      : "memory");
-  }
-}
-
-// Chain of N (2, 4 or 8) MMAs: A from shared memory (ss) or tensor memory (ts).
-template <int N, int KIND>
-__device__ __forceinline__ void mma_chain_ss(uint32_t d, uint32_t idesc, uint32_t acc0,
-                                             const uint64_t (&a)[N], const uint64_t (&b)[N]) {
-  static_assert(N == 2 || N == 4 || N == 8, "MMA chain length");
-  if constexpr (N == 2)
-    mma_chain_ss2<KIND>(d, idesc, acc0, a, b);
-  else if constexpr (N == 4)
-    mma_chain_ss4<KIND>(d, idesc, acc0, a, b);
-  else
-    mma_chain_ss8<KIND>(d, idesc, acc0, a, b);
-}
-
-template <int N, int KIND>
-__device__ __forceinline__ void mma_chain_ts(uint32_t d, uint32_t idesc, uint32_t acc0,
-                                             const uint32_t (&a)[N], const uint64_t (&b)[N]) {
-  static_assert(N == 2 || N == 4 || N == 8, "MMA chain length");
-  if constexpr (N == 2)
-    mma_chain_ts2<KIND>(d, idesc, acc0, a, b);
-  else if constexpr (N == 4)
-    mma_chain_ts4<KIND>(d, idesc, acc0, a, b);
-  else
-    mma_chain_ts8<KIND>(d, idesc, acc0, a, b);
-}
-
-// ---- MMA chains from base descriptors: the per-MMA descriptors are the base plus immediate
+// ---- MMA chains: all MMAs of one product in one asm block.  Issued this way the tensor core
+// runs the attention kernel's S / P V alternation at its full rate (64 cycles per 128x128x16
+// bf16 MMA, measured); the same MMAs issued one asm statement at a time ran at 92-113 cycles.
+// The first MMA accumulates into D when acc0 != 0, the others always accumulate.  KIND: 0 =
+// kind::f16, 1 = kind::f8f6f4.  The per-MMA descriptors are a base plus immediate
 // offsets (template arguments, in 16-byte units for shared-memory descriptors and in columns
 // for tensor-memory A operands), formed inside the asm block, so only the bases occupy
 // registers in the issuing thread.  Offsets of MMAs past N are ignored.
@@ -638,14 +430,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-      : EXATTN_R8(0), EXATTN_R8(8)
-      : "r"(taddr));
-}
-
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -749,13 +533,13 @@ __device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
   return r;
 }
 __device__ __forceinline__ float f32x2_lo(uint64_t v) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  float lo;
+  asm("{\n\t.reg .f32 t;\n\tmov.b64 {%0, t}, %1;\n\t}" : "=f"(lo) : "l"(v));
   return lo;
 }
 __device__ __forceinline__ float f32x2_hi(uint64_t v) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  float hi;
+  asm("{\n\t.reg .f32 t;\n\tmov.b64 {t, %0}, %1;\n\t}" : "=f"(hi) : "l"(v));
   return hi;
 }
 __device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
@@ -810,12 +594,6 @@ __device__ __forceinline__ float ex2_poly(float x) {
 __device__ __forceinline__ float lg2_mufu(float x) {
   float y;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ float rcp_mufu(float x) {
-  float y;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
