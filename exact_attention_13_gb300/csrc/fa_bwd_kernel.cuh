@@ -358,8 +358,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     } else if (warp == 9) {
       // ------------------------------------------------------------ MMA issuer
-      if (lane == 0) {
-        bool ok = wait_phase(smem_u32(&ctl->fix_full), 0, abort_flag, status);
+      // The whole warp runs the issue loop (warp-uniform descriptor arithmetic); one elected
+      // lane issues each product and commit.  Wait outcomes are made warp-uniform.
+      {
+        auto mwait = [&](uint32_t bar, uint32_t parity) -> bool {
+          return __all_sync(0xffffffffu, wait_phase(bar, parity, abort_flag, status));
+        };
+        bool ok = mwait(smem_u32(&ctl->fix_full), 0);
         tc_fence_after();
         const uint32_t k_tile = smem_u32(s_k), v_tile = smem_u32(s_v);
         // Issue order per step u: dV(u), S(u+1), dK(u), dP(u+1).  S(u+1) overwrites P^T(u)
@@ -369,40 +374,52 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         auto tile = [&](int u, int which) {
           return smem_u32(s_ring + (2 * (u & 1) + which) * G::kTileBytes);
         };
-        ok = ok && wait_phase(smem_u32(&ctl->ring_full[0]), 0, abort_flag, status);
+        ok = ok && mwait(smem_u32(&ctl->ring_full[0]), 0);
         if (ok) {
           tc_fence_after();
-          mma_s_type<D>(tmem, k_tile, tile(0, 0));          // S^T  = K_j Q_i^T
-          tc_commit(smem_u32(&ctl->s_full));
-          mma_s_type<D>(tmem + 128, v_tile, tile(0, 1));    // dP^T = V_j dO_i^T
-          tc_commit(smem_u32(&ctl->dp_full));
+          if (elect_one()) {
+            mma_s_type<D>(tmem, k_tile, tile(0, 0));          // S^T  = K_j Q_i^T
+            tc_commit(smem_u32(&ctl->s_full));
+            mma_s_type<D>(tmem + 128, v_tile, tile(0, 1));    // dP^T = V_j dO_i^T
+            tc_commit(smem_u32(&ctl->dp_full));
+          }
+          __syncwarp();
         }
         for (int u = 0; u < nq && ok; ++u) {
           const bool more = u + 1 < nq;
-          ok = wait_phase(smem_u32(&ctl->p_full), u & 1, abort_flag, status);
+          ok = mwait(smem_u32(&ctl->p_full), u & 1);
           if (!ok) break;
           tc_fence_after();
-          mma_acc<D>(tmem + 256, tmem, tile(u, 1), u > 0);         // dV += P^T dO_i
+          if (elect_one()) mma_acc<D>(tmem + 256, tmem, tile(u, 1), u > 0);   // dV += P^T dO_i
+          __syncwarp();
           if (more) {
-            ok = wait_phase(smem_u32(&ctl->ring_full[(u + 1) & 1]), ((u + 1) >> 1) & 1, abort_flag,
-                            status);
+            ok = mwait(smem_u32(&ctl->ring_full[(u + 1) & 1]), ((u + 1) >> 1) & 1);
             if (!ok) break;
             tc_fence_after();
-            mma_s_type<D>(tmem, k_tile, tile(u + 1, 0));
-            tc_commit(smem_u32(&ctl->s_full));
+            if (elect_one()) {
+              mma_s_type<D>(tmem, k_tile, tile(u + 1, 0));
+              tc_commit(smem_u32(&ctl->s_full));
+            }
+            __syncwarp();
           }
-          ok = wait_phase(smem_u32(&ctl->ds_full), u & 1, abort_flag, status);
+          ok = mwait(smem_u32(&ctl->ds_full), u & 1);
           if (!ok) break;
           tc_fence_after();
-          mma_acc<D>(tmem + 384, tmem + 128, tile(u, 0), u > 0);   // dK += dS^T Q_i
-          tc_commit(smem_u32(&ctl->ring_empty[u & 1]));
-          if (more) {
-            mma_s_type<D>(tmem + 128, v_tile, tile(u + 1, 1));
-            tc_commit(smem_u32(&ctl->dp_full));
+          if (elect_one()) {
+            mma_acc<D>(tmem + 384, tmem + 128, tile(u, 0), u > 0);   // dK += dS^T Q_i
+            tc_commit(smem_u32(&ctl->ring_empty[u & 1]));
+            if (more) {
+              mma_s_type<D>(tmem + 128, v_tile, tile(u + 1, 1));
+              tc_commit(smem_u32(&ctl->dp_full));
+            }
           }
+          __syncwarp();
         }
-        if (ok) tc_commit(smem_u32(&ctl->o_full));
-        tc_commit(smem_u32(&ctl->drain));
+        if (elect_one()) {
+          if (ok) tc_commit(smem_u32(&ctl->o_full));
+          tc_commit(smem_u32(&ctl->drain));
+        }
+        __syncwarp();
         const uint64_t t0 = globaltimer_ns();
         while (!mbar_try_wait(smem_u32(&ctl->drain), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
         }
@@ -622,8 +639,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
     } else if (warp == 9) {
-      if (lane == 0) {
-        bool ok = wait_phase(smem_u32(&ctl->fix_full), 0, abort_flag, status);
+      // The whole warp runs the issue loop; one elected lane issues (as in the dK/dV kernel).
+      {
+        auto mwait = [&](uint32_t bar, uint32_t parity) -> bool {
+          return __all_sync(0xffffffffu, wait_phase(bar, parity, abort_flag, status));
+        };
+        bool ok = mwait(smem_u32(&ctl->fix_full), 0);
         tc_fence_after();
         const uint32_t q_tile = smem_u32(s_q), do_tile = smem_u32(s_do);
         // Issue order per step u: S(u+1) once the softmax has read S(u), then dQ(u), dP(u+1);
@@ -631,48 +652,65 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // back behind dP, K_j's behind dQ.
         auto tile = [&](int t) { return smem_u32(s_ring + (t % kDqSlots) * G::kTileBytes); };
         auto tile_ready = [&](int t) {
-          const bool r = wait_phase(smem_u32(&ctl->tile_full[t % kDqSlots]), (t / kDqSlots) & 1,
-                                    abort_flag, status);
+          const bool r = mwait(smem_u32(&ctl->tile_full[t % kDqSlots]), (t / kDqSlots) & 1);
           tc_fence_after();
           return r;
         };
         auto release = [&](int t) { tc_commit(smem_u32(&ctl->tile_empty[t % kDqSlots])); };
         ok = ok && tile_ready(0);
         if (ok) {
-          mma_s_type<D>(tmem, q_tile, tile(0));           // S  = Q_i K_j^T
-          tc_commit(smem_u32(&ctl->s_full));
+          if (elect_one()) {
+            mma_s_type<D>(tmem, q_tile, tile(0));           // S  = Q_i K_j^T
+            tc_commit(smem_u32(&ctl->s_full));
+          }
+          __syncwarp();
           ok = tile_ready(1);
         }
         if (ok) {
-          mma_s_type<D>(tmem + 128, do_tile, tile(1));    // dP = dO_i V_j^T
-          tc_commit(smem_u32(&ctl->dp_full));
-          release(1);
+          if (elect_one()) {
+            mma_s_type<D>(tmem + 128, do_tile, tile(1));    // dP = dO_i V_j^T
+            tc_commit(smem_u32(&ctl->dp_full));
+            release(1);
+          }
+          __syncwarp();
         }
         for (int u = 0; u < nk && ok; ++u) {
           const bool more = u + 1 < nk;
           if (more) {
-            ok = wait_phase(smem_u32(&ctl->p_full), u & 1, abort_flag, status);
+            ok = mwait(smem_u32(&ctl->p_full), u & 1);
             if (ok) ok = tile_ready(2 * u + 2);
             if (!ok) break;
             tc_fence_after();
-            mma_s_type<D>(tmem, q_tile, tile(2 * u + 2));
-            tc_commit(smem_u32(&ctl->s_full));
+            if (elect_one()) {
+              mma_s_type<D>(tmem, q_tile, tile(2 * u + 2));
+              tc_commit(smem_u32(&ctl->s_full));
+            }
+            __syncwarp();
           }
-          ok = wait_phase(smem_u32(&ctl->ds_full), u & 1, abort_flag, status);
+          ok = mwait(smem_u32(&ctl->ds_full), u & 1);
           if (!ok) break;
           tc_fence_after();
-          mma_acc<D>(tmem + 256, tmem + 128, tile(2 * u), u > 0);   // dQ += dS K_j
-          release(2 * u);
+          if (elect_one()) {
+            mma_acc<D>(tmem + 256, tmem + 128, tile(2 * u), u > 0);   // dQ += dS K_j
+            release(2 * u);
+          }
+          __syncwarp();
           if (more) {
             ok = tile_ready(2 * u + 3);
             if (!ok) break;
-            mma_s_type<D>(tmem + 128, do_tile, tile(2 * u + 3));
-            tc_commit(smem_u32(&ctl->dp_full));
-            release(2 * u + 3);
+            if (elect_one()) {
+              mma_s_type<D>(tmem + 128, do_tile, tile(2 * u + 3));
+              tc_commit(smem_u32(&ctl->dp_full));
+              release(2 * u + 3);
+            }
+            __syncwarp();
           }
         }
-        if (ok) tc_commit(smem_u32(&ctl->o_full));
-        tc_commit(smem_u32(&ctl->drain));
+        if (elect_one()) {
+          if (ok) tc_commit(smem_u32(&ctl->o_full));
+          tc_commit(smem_u32(&ctl->drain));
+        }
+        __syncwarp();
         const uint64_t t0 = globaltimer_ns();
         while (!mbar_try_wait(smem_u32(&ctl->drain), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
         }

@@ -15,7 +15,7 @@
 //                                    end normalises O, stores it and the row's log-sum-exp
 //   warp  8    TMA producer          Q tiles once, then K_j, V_j into the ring (full/empty
 //                                    mbarriers, "FlashAttention · InkStack", section 3.2.1)
-//   warp  9    MMA issuer            one thread issues S_h = Q_h K_j^T (both operands in smem)
+//   warp  9    MMA issuer            one elected lane issues S_h = Q_h K_j^T (both operands in smem)
 //                                    and O_h += P_h V_j (P from TMEM, V from smem), and owns the
 //                                    TMEM allocation
 //   warps 10-11 V converters         (fp8 operands with an f16 P V product only) widen each
@@ -506,8 +506,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ============================================================ MMA issuer
-    if (lane == 0 && nkv_load > 0) {
-      bool ok = wait_phase(smem_u32(&ctl->q_full), 0, abort_flag, args.status);
+    if (nkv_load > 0) {
+      // The whole warp runs the issue loop, so the descriptor arithmetic is warp-uniform; one
+      // lane, elected from the converged warp, issues each product and commit.  (With the loop
+      // in lane 0 alone the same MMAs went out measurably slower: headline shape -7 %, causal
+      // head-dim-64 shape -11 %.)
+      auto issuer = []() -> bool { return elect_one(); };
+      // a wait whose outcome every lane agrees on (an abort racing a phase completion could
+      // otherwise split the warp), which also reconverges it
+      auto mwait = [&](uint32_t bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, wait_phase(bar, parity, abort_flag, args.status));
+      };
+      bool ok = mwait(smem_u32(&ctl->q_full), 0);
       tc_fence_after();
       const uint32_t q_base = smem_u32(s_q);
       const uint32_t ring_base = smem_u32(s_ring);
@@ -518,8 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // warps of its SMSP) leaves the pipe idle.  Each step therefore does its waits first, then
       // issues P V and the next S back to back with descriptors formed from per-tile bases.
       auto wait_kv = [&](int t) -> bool {
-        return wait_phase(smem_u32(&ctl->kv_full[t % G::kSlots]), (t / G::kSlots) & 1,
-                          abort_flag, args.status);
+        return mwait(smem_u32(&ctl->kv_full[t % G::kSlots]), (t / G::kSlots) & 1);
       };
       const uint64_t q_desc = smem_desc(q_base, 16, 8 * G::kSwBytes, G::kSwMode);
       const uint64_t ring_desc = smem_desc(ring_base, 16, 8 * G::kSwBytes, G::kSwMode);
@@ -528,24 +537,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = 2 * j;
         const uint64_t qd = q_desc + static_cast<uint64_t>(h * (G::kTileBytes >> 4));
         const uint64_t kd = ring_desc + static_cast<uint64_t>((t % G::kSlots) * (G::kTileBytes >> 4));
-        mma_chain_ss_off<G::kKStepsS, FP8 ? 1 : 0, G::s_off(1), G::s_off(2), G::s_off(3),
-                         G::s_off(4), G::s_off(5), G::s_off(6), G::s_off(7)>(
-            tmem + h * 128, G::kIdescS, 0u, qd, kd);
-        tc_commit(smem_u32(&ctl->s_full[h]));
+        if (issuer()) {
+          mma_chain_ss_off<G::kKStepsS, FP8 ? 1 : 0, G::s_off(1), G::s_off(2), G::s_off(3),
+                           G::s_off(4), G::s_off(5), G::s_off(6), G::s_off(7)>(
+              tmem + h * 128, G::kIdescS, 0u, qd, kd);
+          tc_commit(smem_u32(&ctl->s_full[h]));
+        }
+        __syncwarp();
         EXATTN_TRACE_EVENT(6, h, j);
       };
       // V_j (or its f16 copy) ready; returns its shared-memory descriptor base
       auto wait_v = [&](int h, int j, uint64_t& vd) -> bool {
         const int t = 2 * j + 1;
         if constexpr (G::kPv16) {
-          if (!wait_phase(smem_u32(&ctl->v16_full[j & 1]), (j >> 1) & 1, abort_flag,
-                          args.status))
-            return false;
+          if (!mwait(smem_u32(&ctl->v16_full[j & 1]), (j >> 1) & 1)) return false;
           vd = smem_desc(smem_u32(s_v16) + (j & 1) * G::kV16TileBytes, kTileRows * G::kPvSwBytes,
                          8 * G::kPvSwBytes, kSwizzle128B);
           // both converter warps are done with the e4m3 copy: hand its slot back
           const bool first_user = (h == 0) || (j >= nkv[0]);
-          if (first_user) mbar_arrive(smem_u32(&ctl->kv_empty[t % G::kSlots]));
+          if (first_user && lane == 0) mbar_arrive(smem_u32(&ctl->kv_empty[t % G::kSlots]));
         } else {
           if (!wait_kv(t)) return false;
           vd = smem_desc(ring_base + (t % G::kSlots) * G::kTileBytes, kTileRows * G::kPvSwBytes,
@@ -559,10 +569,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_pv_part = [&](int h, int j, int half, uint64_t vd) {
         constexpr int kN = G::kPvSteps / kPHalves;   // MMAs per published part of P
         // A: 8 TMEM columns of P per MMA; B: the next key group of V
-        mma_chain_ts_off<kN, G::kPE4m3 ? 1 : 0, G::kPvStep, 8, 16, 24, 32, 40, 48, 56>(
-            tmem + 256 + h * 128, G::kIdescPV, (j > 0 || half > 0) ? 1u : 0u,
-            tmem + h * 128 + half * kN * 8,
-            vd + static_cast<uint64_t>(half * kN * G::kPvStep));
+        if (issuer())
+          mma_chain_ts_off<kN, G::kPE4m3 ? 1 : 0, G::kPvStep, 8, 16, 24, 32, 40, 48, 56>(
+              tmem + 256 + h * 128, G::kIdescPV, (j > 0 || half > 0) ? 1u : 0u,
+              tmem + h * 128 + half * kN * 8,
+              vd + static_cast<uint64_t>(half * kN * G::kPvStep));
+        __syncwarp();
       };
       // one step of tile h: P V of block j, then S of block j + 1 (which overwrites P_h)
       auto step = [&](int h, int j) -> bool {
@@ -573,14 +585,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         EXATTN_TRACE_EVENT(7, h, j + 1);
 #pragma unroll
         for (int half = 0; half < kPHalves; ++half) {
-          if (!wait_phase(smem_u32(&ctl->p_full[h][half]), j & 1, abort_flag, args.status))
-            return false;
+          if (!mwait(smem_u32(&ctl->p_full[h][half]), j & 1)) return false;
           tc_fence_after();
           if (half == 0) EXATTN_TRACE_EVENT(4, h, j);
           issue_pv_part(h, j, half, vd);
         }
         EXATTN_TRACE_EVENT(5, h, j);
-        if (j == nkv[h] - 1) tc_commit(smem_u32(&ctl->o_full[h]));
+        if (j == nkv[h] - 1) {
+          if (issuer()) tc_commit(smem_u32(&ctl->o_full[h]));
+          __syncwarp();
+        }
         if (more) issue_s(h, j + 1);
         return true;
       };
@@ -597,7 +611,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j < nkv[h]) ok = step(h, j);
       }
       // make sure nothing this thread issued is still running before TMEM is released
-      tc_commit(smem_u32(&ctl->drain));
+      __syncwarp();
+      if (issuer()) tc_commit(smem_u32(&ctl->drain));
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(smem_u32(&ctl->drain), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
       }

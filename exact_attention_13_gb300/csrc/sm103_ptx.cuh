@@ -27,6 +27,15 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// One lane of the (converged) warp is elected; warp-collective.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t is_elected;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(is_elected));
+  return is_elected != 0;
+}
+
 // Register budget moves between warpgroups (all warps of a warpgroup execute the same one).
 template <int N>
 __device__ __forceinline__ void regs_inc() {
