@@ -546,24 +546,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         EXATTN_TRACE_EVENT(6, h, j);
       };
-      // V_j (or its f16 copy) ready; returns its shared-memory descriptor base
-      auto wait_v = [&](int h, int j, uint64_t& vd) -> bool {
-        const int t = 2 * j + 1;
-        if constexpr (G::kPv16) {
-          if (!mwait(smem_u32(&ctl->v16_full[j & 1]), (j >> 1) & 1)) return false;
-          vd = smem_desc(smem_u32(s_v16) + (j & 1) * G::kV16TileBytes, kTileRows * G::kPvSwBytes,
-                         8 * G::kPvSwBytes, kSwizzle128B);
-          // both converter warps are done with the e4m3 copy: hand its slot back
-          const bool first_user = (h == 0) || (j >= nkv[0]);
-          if (first_user && lane == 0) mbar_arrive(smem_u32(&ctl->kv_empty[t % G::kSlots]));
-        } else {
-          if (!wait_kv(t)) return false;
-          vd = smem_desc(ring_base + (t % G::kSlots) * G::kTileBytes, kTileRows * G::kPvSwBytes,
-                         8 * G::kPvSwBytes, G::kSwMode);
-        }
-        EXATTN_TRACE_EVENT(8, h, j);
-        return true;
-      };
       // O_h += P_h V_j, P_h read from TMEM over S_h's columns.  The softmax may publish P in two
       // halves of 64 keys; the MMAs of the first half start while the second is computed.
       auto issue_pv_part = [&](int h, int j, int half, uint64_t vd) {
@@ -576,16 +558,39 @@ __global__ void __launch_bounds__(kThreads, 1)
               vd + static_cast<uint64_t>(half * kN * G::kPvStep));
         __syncwarp();
       };
-      // one step of tile h: P V of block j, then S of block j + 1 (which overwrites P_h)
+      // one step of tile h: P V of block j, then S of block j + 1 (which overwrites P_h).  It
+      // needs V_j (or its f16 copy), K_{j+1} and (the first part of) P_h(j); the first two have
+      // almost always landed and P_h(j) is often published already, so one probe checks all
+      // three at once and the waits run one by one only when one of them is still open.
       auto step = [&](int h, int j) -> bool {
         const bool more = j + 1 < nkv[h];
+        const int tv = 2 * j + 1, tk = 2 * j + 2;
+        const uint32_t bar_v = G::kPv16 ? smem_u32(&ctl->v16_full[j & 1])
+                                        : smem_u32(&ctl->kv_full[tv % G::kSlots]);
+        const uint32_t par_v = G::kPv16 ? (j >> 1) & 1 : (tv / G::kSlots) & 1;
+        const uint32_t bar_k = more ? smem_u32(&ctl->kv_full[tk % G::kSlots]) : bar_v;
+        const uint32_t par_k = more ? (tk / G::kSlots) & 1 : par_v;
+        const uint32_t bar_p = smem_u32(&ctl->p_full[h][0]);
+        const uint32_t par_p = j & 1;
+        if (!__all_sync(0xffffffffu, mbar_try_wait3(bar_v, par_v, bar_k, par_k, bar_p, par_p))) {
+          if (!mwait(bar_v, par_v) || !mwait(bar_k, par_k) || !mwait(bar_p, par_p)) return false;
+        }
+        EXATTN_TRACE_EVENT(8, h, j);
         uint64_t vd;
-        if (!wait_v(h, j, vd)) return false;
-        if (more && !wait_kv(2 * (j + 1))) return false;
+        if constexpr (G::kPv16) {
+          vd = smem_desc(smem_u32(s_v16) + (j & 1) * G::kV16TileBytes, kTileRows * G::kPvSwBytes,
+                         8 * G::kPvSwBytes, kSwizzle128B);
+          // both converter warps are done with the e4m3 copy: hand its slot back
+          const bool first_user = (h == 0) || (j >= nkv[0]);
+          if (first_user && lane == 0) mbar_arrive(smem_u32(&ctl->kv_empty[tv % G::kSlots]));
+        } else {
+          vd = smem_desc(ring_base + (tv % G::kSlots) * G::kTileBytes, kTileRows * G::kPvSwBytes,
+                         8 * G::kPvSwBytes, G::kSwMode);
+        }
         EXATTN_TRACE_EVENT(7, h, j + 1);
 #pragma unroll
         for (int half = 0; half < kPHalves; ++half) {
-          if (!mwait(smem_u32(&ctl->p_full[h][half]), j & 1)) return false;
+          if (half > 0 && !mwait(smem_u32(&ctl->p_full[h][half]), j & 1)) return false;
           tc_fence_after();
           if (half == 0) EXATTN_TRACE_EVENT(4, h, j);
           issue_pv_part(h, j, half, vd);

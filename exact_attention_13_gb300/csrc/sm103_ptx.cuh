@@ -83,6 +83,24 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
   return done;
 }
 
+// Three phases probed at once (independent try_waits in one block, so their latencies overlap);
+// nonzero when all three have completed.
+__device__ __forceinline__ uint32_t mbar_try_wait3(uint32_t b0, uint32_t p0, uint32_t b1,
+                                                   uint32_t p1, uint32_t b2, uint32_t p2) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred q0, q1, q2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 q2, [%5], %6;\n\t"
+      "and.pred q0, q0, q1;\n\tand.pred q0, q0, q2;\n\t"
+      "selp.u32 %0, 1, 0, q0;\n\t}"
+      : "=r"(done)
+      : "r"(b0), "r"(p0), "r"(b1), "r"(p1), "r"(b2), "r"(p2)
+      : "memory");
+  return done;
+}
+
 // ------------------------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor)
 // ------------------------------------------------------------------------------------------
