@@ -192,11 +192,11 @@ __device__ __forceinline__ void softmax_p(uint32_t t_s, float c, const float* l2
       for (int i = 0; i < 32; ++i) lv[i] = l2_row;
     }
     if (pass == 1) tmem_ld_wait();
-    const uint64_t c2 = f32x2(c, c);
+    const float2 c2 = f32x2(c, c);
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
       // s c - LSE log2(e) for two columns in one packed fma
-      const uint64_t x2 = fma_f32x2(f32x2(__uint_as_float(rs[pass][i]), __uint_as_float(rs[pass][i + 1])),
+      const float2 x2 = fma_f32x2(f32x2(__uint_as_float(rs[pass][i]), __uint_as_float(rs[pass][i + 1])),
                                     c2, f32x2(-lv[i], -lv[i + 1]));
       float x0 = ex2_mufu(f32x2_lo(x2)), x1 = ex2_mufu(f32x2_hi(x2));
       if constexpr (MASKED) {
@@ -246,9 +246,9 @@ __device__ __forceinline__ void softmax_ds(uint32_t t_dp, const float* dl, float
     for (int i = 0; i < 16; ++i) {
       const int q = 32 * pass + 2 * i;
       // dS = P (dP - D), two columns per packed add and multiply
-      const uint64_t t2 = add_f32x2(f32x2(__uint_as_float(rd[pass][2 * i]), __uint_as_float(rd[pass][2 * i + 1])),
+      const float2 t2 = add_f32x2(f32x2(__uint_as_float(rd[pass][2 * i]), __uint_as_float(rd[pass][2 * i + 1])),
                                     f32x2(-dv[2 * i], -dv[2 * i + 1]));
-      const uint64_t d2 = mul_f32x2(f32x2(p[q], p[q + 1]), t2);
+      const float2 d2 = mul_f32x2(f32x2(p[q], p[q + 1]), t2);
       pd[i] = pack_bf16x2(f32x2_lo(d2), f32x2_hi(d2));
     }
     tmem_st16(t_dp + 16 * pass, pd);

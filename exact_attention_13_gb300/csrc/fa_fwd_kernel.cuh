@@ -310,13 +310,13 @@ __device__ __forceinline__ float exp_and_publish(float (&s)[128], float c, float
                                                  int lane) {
   // eight partial sums (element i goes to sum i % 8), kept as four packed pairs; the exponent
   // arguments s c - m are formed two at a time (same rounding as the scalar fma)
-  uint64_t ps2[4] = {0ull, 0ull, 0ull, 0ull};
-  const uint64_t c2 = f32x2(c, c), nm2 = f32x2(-m, -m);
+  float2 ps2[4] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f), f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
+  const float2 c2 = f32x2(c, c), nm2 = f32x2(-m, -m);
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
 #pragma unroll
     for (int i = 64 * half; i < 64 * half + 64; i += 2) {
-      const uint64_t x2 = fma_f32x2(f32x2(s[i], s[i + 1]), c2, nm2);
+      const float2 x2 = fma_f32x2(f32x2(s[i], s[i + 1]), c2, nm2);
       const float x0 = f32x2_lo(x2), x1 = f32x2_hi(x2);
       float p0, p1;
       if constexpr (MASKED) {
@@ -796,10 +796,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cb = 0; cb < D / 32; ++cb) {
           tmem_ld32(t_o + cb * 32, r);
           tmem_ld_wait();
-          const uint64_t a2 = f32x2(alpha, alpha);
+          const float2 a2 = f32x2(alpha, alpha);
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            const uint64_t v = mul_f32x2(f32x2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), a2);
+            const float2 v = mul_f32x2(f32x2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), a2);
             r[i] = __float_as_uint(f32x2_lo(v));
             r[i + 1] = __float_as_uint(f32x2_hi(v));
           }

@@ -552,38 +552,18 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
   return r;
 }
 
-// Packed fp32 pairs (a 64-bit register pair): Blackwell executes fma/add/mul on both halves in
-// one instruction, each half rounded exactly as the scalar operation.
-__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
+// Packed fp32 pairs: Blackwell executes fma/add/mul on both halves of a register pair in one
+// instruction, each half rounded exactly as the scalar operation.  The compiler's float2
+// builtins are used (not inline asm), so it can place the pairs in registers itself.
+__device__ __forceinline__ float2 f32x2(float lo, float hi) { return make_float2(lo, hi); }
+__device__ __forceinline__ float f32x2_lo(float2 v) { return v.x; }
+__device__ __forceinline__ float f32x2_hi(float2 v) { return v.y; }
+__device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c) {
+  return __ffma2_rn(a, b, c);
 }
-__device__ __forceinline__ float f32x2_lo(uint64_t v) {
-  float lo;
-  asm("{\n\t.reg .f32 t;\n\tmov.b64 {%0, t}, %1;\n\t}" : "=f"(lo) : "l"(v));
-  return lo;
-}
-__device__ __forceinline__ float f32x2_hi(uint64_t v) {
-  float hi;
-  asm("{\n\t.reg .f32 t;\n\tmov.b64 {t, %0}, %1;\n\t}" : "=f"(hi) : "l"(v));
-  return hi;
-}
-__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
+__device__ __forceinline__ float2 add_f32x2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+
 // max of three floats in one instruction
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float r;
