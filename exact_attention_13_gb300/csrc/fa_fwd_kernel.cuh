@@ -162,9 +162,8 @@ __device__ __forceinline__ float round_p(float p) {
 }
 
 // Design knobs (compile-time).  The defaults are the measured best on GB300 (A/B over whole
-// launches of the headline shapes): bf16 is MMA-issue-bound and prefers P published in one
-// part with a short L2 prefetch; e4m3 is softmax-bound and gains from PV starting on the first
-// half of P and a deeper prefetch.  -D overrides apply to both operand types.
+// launches of the headline shapes): bf16 prefers a short L2 prefetch, e4m3 (softmax-bound) a
+// deeper one.  -D overrides apply to both operand types.
 #ifndef EXATTN_KV_SLOTS_D128
 #define EXATTN_KV_SLOTS_D128 4
 #endif
@@ -179,14 +178,10 @@ __host__ __device__ constexpr int l2_prefetch_blocks() {
   return FP8 ? 6 : 2;
 #endif
 }
-template <bool FP8>
-__host__ __device__ constexpr int p_parts() {
-#ifdef EXATTN_P_HALVES
-  return EXATTN_P_HALVES;
-#else
-  return FP8 ? 2 : 1;
-#endif
-}
+// P is published in two parts of 64 keys: the P V MMAs of the first part run while the softmax
+// computes the second.  (For bf16 P this measured -3 % while the MMA issue was the bottleneck;
+// with the issue loop run by the whole warp it is +6 % on the headline shape.)
+__host__ __device__ constexpr int p_parts() { return 2; }
 
 struct KernelArgs {
   __nv_bfloat16* o;   // [BH, N, d]            (one key split)
@@ -375,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap map_v, const KernelArgs args) {
   using G = Geo<D, FP8, PV16>;
   constexpr PFmt kPFmt = p_fmt<FP8, PV16>();
-  constexpr int kPHalves = p_parts<FP8>();
+  constexpr int kPHalves = p_parts();
   constexpr int kL2PrefetchBlocks = l2_prefetch_blocks<FP8>();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &

@@ -1,7 +1,7 @@
 """Parity of the forward kernel's compile-time variants against the fp64 oracle.
 
-The library ships one schedule; two alternatives stay in the kernel source as compile-time knobs
-and are built here into libraries of their own, so that neither can rot unnoticed:
+The library ships one schedule; the alternatives stay in the kernel source as compile-time knobs
+and are built here into libraries of their own, so that none can rot unnoticed:
 
 * ``EXATTN_EMU_EVERY=2``: every second exponential of an unmasked key block is evaluated by the
   FMA polynomial instead of MUFU (the partial emulation of "FlashAttention4 精读", section 3.1.3;
@@ -10,6 +10,9 @@ and are built here into libraries of their own, so that neither can rot unnotice
   rescale bf16 rows whenever the max grows: the lazy threshold needs every column on MUFU.)
 * ``EXATTN_RESCALE_LOG2=0``: the exact online-softmax schedule for bf16 P, O rescaled whenever
   a row's max grows, instead of the lazy threshold of 8 of section 3.1.4.
+* ``EXATTN_KV_SLOTS_D128=5 EXATTN_L2_PREFETCH_BLOCKS=4``: the tuning knobs of the K/V ring (an
+  odd number of slots, so K and V blocks alternate between slots) and of the L2 prefetch
+  distance.
 
 Each variant runs the small benchmark shape, the causal shape with Q scaled by 8 (logits over
 about +-100, the rescale stress case), a ragged causal head-dim-64 shape and two fp8 shapes, at
@@ -29,6 +32,7 @@ pytestmark = pytest.mark.gpu
 VARIANTS = {
     "emu2": ["-DEXATTN_EMU_EVERY=2"],
     "rescale0": ["-DEXATTN_RESCALE_LOG2=0.0f"],
+    "ring5_pf4": ["-DEXATTN_KV_SLOTS_D128=5", "-DEXATTN_L2_PREFETCH_BLOCKS=4"],
 }
 
 
