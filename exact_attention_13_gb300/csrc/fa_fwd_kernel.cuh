@@ -180,7 +180,8 @@ __host__ __device__ constexpr int l2_prefetch_blocks() {
 }
 // P is published in two parts of 64 keys: the P V MMAs of the first part run while the softmax
 // computes the second.  (For bf16 P this measured -3 % while the MMA issue was the bottleneck;
-// with the issue loop run by the whole warp it is +6 % on the headline shape.)
+// with the issue loop run by the whole warp it is +6 % on the headline shape.  Four parts of
+// 32 keys measured 9-18 % slower: every part adds a hand-off to both sides.)
 __host__ __device__ constexpr int p_parts() { return 2; }
 
 struct KernelArgs {
@@ -250,7 +251,7 @@ struct Ctrl {
   uint64_t kv_full[kSlots];
   uint64_t kv_empty[kSlots];
   uint64_t s_full[2];
-  uint64_t p_full[2][2];  // [tile][half of the keys]
+  uint64_t p_full[2][p_parts()];  // [tile][published part of the keys]
   uint64_t o_full[2];
   uint64_t v16_full[2];   // f16 V buffer b written (PV16)
   uint64_t v16_empty[2];  // f16 V buffer b no longer read by the MMAs (PV16)
@@ -296,21 +297,22 @@ __device__ __forceinline__ int kv_blocks_for_tile(int row0, int n) {
 // Softmax numerator of one row: p_i = 2^(s_i c - m) for the 128 keys of the block (keys >= lim
 // are masked to 0 when MASKED; with EMU_EVERY > 0 one column in EMU_EVERY of an unmasked block
 // uses the FMA polynomial, "FlashAttention4 精读", section 3.1.3 "partial emulation"), rounded
-// to bf16 (or e4m3) and written over the S columns in TMEM in two halves of 64 keys; after the
-// last half (or after each half when P_PARTS == 2) the warp publishes on the P barrier.  Returns
-// the fp32 sum of the unrounded p.
+// to bf16 (or f16 or e4m3) and written over the S columns in TMEM in two parts of 64 keys; after
+// each part the warp publishes on that part's P barrier.  Returns the fp32 sum of the unrounded
+// p.
 template <bool MASKED, PFmt PF, int P_PARTS, int EMU_EVERY>
 __device__ __forceinline__ float exp_and_publish(float (&s)[128], float c, float m, int lim,
-                                                 uint32_t t_s, uint32_t bar0, uint32_t bar1,
-                                                 int lane) {
+                                                 uint32_t t_s, uint32_t bar0, int lane) {
+  static_assert(P_PARTS == 2, "P is published in two parts of 64 keys");
+  constexpr int kKeys = 128 / P_PARTS;   // keys per published part
   // eight partial sums (element i goes to sum i % 8), kept as four packed pairs; the exponent
   // arguments s c - m are formed two at a time (same rounding as the scalar fma)
   float2 ps2[4] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f), f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
   const float2 c2 = f32x2(c, c), nm2 = f32x2(-m, -m);
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
+  for (int part = 0; part < P_PARTS; ++part) {
 #pragma unroll
-    for (int i = 64 * half; i < 64 * half + 64; i += 2) {
+    for (int i = kKeys * part; i < kKeys * part + kKeys; i += 2) {
       const float2 x2 = fma_f32x2(f32x2(s[i], s[i + 1]), c2, nm2);
       const float x0 = f32x2_lo(x2), x1 = f32x2_hi(x2);
       float p0, p1;
@@ -329,27 +331,28 @@ __device__ __forceinline__ float exp_and_publish(float (&s)[128], float c, float
       ps2[(i / 2) % 4] = add_f32x2(ps2[(i / 2) % 4], f32x2(p0, p1));
     }
     if constexpr (PF == PFmt::kE4m3) {
-      uint32_t r[16];
+      // four keys per TMEM column
+      uint32_t r[kKeys / 4];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int k = 64 * half + 4 * i;
+      for (int i = 0; i < kKeys / 4; ++i) {
+        const int k = kKeys * part + 4 * i;
         r[i] = pack_e4m3x4(s[k], s[k + 1], s[k + 2], s[k + 3]);
       }
-      tmem_st16(t_s + 16 * half, r);
+      tmem_st16(t_s + 16 * part, r);
     } else {
-      uint32_t r[32];
+      // two keys per TMEM column
+      uint32_t r[kKeys / 2];
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        r[i] = PF == PFmt::kF16 ? pack_f16x2(s[64 * half + 2 * i], s[64 * half + 2 * i + 1])
-                                : pack_bf16x2(s[64 * half + 2 * i], s[64 * half + 2 * i + 1]);
-      tmem_st32(t_s + 32 * half, r);
+      for (int i = 0; i < kKeys / 2; ++i) {
+        const int k = kKeys * part + 2 * i;
+        r[i] = PF == PFmt::kF16 ? pack_f16x2(s[k], s[k + 1]) : pack_bf16x2(s[k], s[k + 1]);
+      }
+      tmem_st32(t_s + 32 * part, r);
     }
-    if (P_PARTS == 2 || half == 1) {
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(half == 0 ? bar0 : bar1);
-    }
+    tmem_st_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar0 + 8 * part);   // p_full[h][part]
   }
   float ps[8];
 #pragma unroll
@@ -416,8 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(smem_u32(&ctl->s_full[h]), 1);
-      mbar_init(smem_u32(&ctl->p_full[h][0]), 4);  // one arrival per softmax warp
-      mbar_init(smem_u32(&ctl->p_full[h][1]), 4);
+      for (int q = 0; q < p_parts(); ++q)
+        mbar_init(smem_u32(&ctl->p_full[h][q]), 4);  // one arrival per softmax warp
       mbar_init(smem_u32(&ctl->o_full[h]), 1);
       mbar_init(smem_u32(&ctl->v16_full[h]), 2);  // one arrival per converter warp
       mbar_init(smem_u32(&ctl->v16_empty[h]), 1);
@@ -546,11 +549,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_pv_part = [&](int h, int j, int half, uint64_t vd) {
         constexpr int kN = G::kPvSteps / kPHalves;   // MMAs per published part of P
         // A: 8 TMEM columns of P per MMA; B: the next key group of V
+        const uint32_t acc = (j > 0 || half > 0) ? 1u : 0u;
+        const uint32_t a_tm = tmem + h * 128 + half * kN * 8;
+        const uint64_t b_desc = vd + static_cast<uint64_t>(half * kN * G::kPvStep);
         if (issuer())
           mma_chain_ts_off<kN, G::kPE4m3 ? 1 : 0, G::kPvStep, 8, 16, 24, 32, 40, 48, 56>(
-              tmem + 256 + h * 128, G::kIdescPV, (j > 0 || half > 0) ? 1u : 0u,
-              tmem + h * 128 + half * kN * 8,
-              vd + static_cast<uint64_t>(half * kN * G::kPvStep));
+              tmem + 256 + h * 128, G::kIdescPV, acc, a_tm, b_desc);
         __syncwarp();
       };
       // one step of tile h: P V of block j, then S of block j + 1 (which overwrites P_h).  It
@@ -809,7 +813,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // probabilities p = 2^(s c - m), written over S (masked keys give exactly 0); the mask
       // test lives in its own instantiation so unmasked blocks run a select-free loop
       const uint32_t pb0 = smem_u32(&ctl->p_full[h][0]);
-      const uint32_t pb1 = smem_u32(&ctl->p_full[h][kPHalves == 2 ? 1 : 0]);
       const float m_shift = m_run - bias_j;
       // The P V product sums the probabilities as rounded to P's format, l_run sums them
       // unrounded.  Where a row's weight sits on one key, that key's rounding would reach O
@@ -823,10 +826,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         l_fix = fmaf(round_p<kPFmt>(p_top) - p_top, l_mult, l_fix);
       }
       const float rowsum =
-          masked ? exp_and_publish<true, kPFmt, kPHalves, 0>(s, c_j, m_shift, lim, t_s, pb0, pb1,
-                                                             lane)
+          masked ? exp_and_publish<true, kPFmt, kPHalves, 0>(s, c_j, m_shift, lim, t_s, pb0, lane)
                  : exp_and_publish<false, kPFmt, kPHalves, EXATTN_EMU_EVERY>(s, c_j, m_shift, lim,
-                                                                             t_s, pb0, pb1, lane);
+                                                                             t_s, pb0, lane);
       if (threadIdx.x % 128 == 0) EXATTN_TRACE_EVENT(3, h, j);
       l_run = fmaf(rowsum, l_mult, l_run);
     }
