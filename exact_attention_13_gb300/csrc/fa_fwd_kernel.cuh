@@ -253,6 +253,8 @@ struct Ctrl {
   uint64_t s_full[2];
   uint64_t p_full[2][p_parts()];  // [tile][published part of the keys]
   uint64_t o_full[2];
+  uint64_t s_read[2];     // the softmax warps of tile h have read S_h (head dim 64)
+  uint64_t pv_done[2];    // P V of tile h's current block complete (head dim 64)
   uint64_t v16_full[2];   // f16 V buffer b written (PV16)
   uint64_t v16_empty[2];  // f16 V buffer b no longer read by the MMAs (PV16)
   uint64_t drain;
@@ -297,12 +299,13 @@ __device__ __forceinline__ int kv_blocks_for_tile(int row0, int n) {
 // Softmax numerator of one row: p_i = 2^(s_i c - m) for the 128 keys of the block (keys >= lim
 // are masked to 0 when MASKED; with EMU_EVERY > 0 one column in EMU_EVERY of an unmasked block
 // uses the FMA polynomial, "FlashAttention4 精读", section 3.1.3 "partial emulation"), rounded
-// to bf16 (or f16 or e4m3) and written over the S columns in TMEM in two parts of 64 keys; after
-// each part the warp publishes on that part's P barrier.  Returns the fp32 sum of the unrounded
-// p.
-template <bool MASKED, PFmt PF, int P_PARTS, int EMU_EVERY>
+// to bf16 (or f16 or e4m3) and written to P's TMEM columns (t_s) in two parts of 64 keys; after
+// each part the warp publishes on that part's P barrier.  pre_store() runs before the first store.
+// Returns the fp32 sum of the unrounded p.
+template <bool MASKED, PFmt PF, int P_PARTS, int EMU_EVERY, typename PreStore>
 __device__ __forceinline__ float exp_and_publish(float (&s)[128], float c, float m, int lim,
-                                                 uint32_t t_s, uint32_t bar0, int lane) {
+                                                 uint32_t t_s, uint32_t bar0, int lane,
+                                                 PreStore&& pre_store) {
   static_assert(P_PARTS == 2, "P is published in two parts of 64 keys");
   constexpr int kKeys = 128 / P_PARTS;   // keys per published part
   // eight partial sums (element i goes to sum i % 8), kept as four packed pairs; the exponent
@@ -330,6 +333,7 @@ __device__ __forceinline__ float exp_and_publish(float (&s)[128], float c, float
       s[i + 1] = p1;
       ps2[(i / 2) % 4] = add_f32x2(ps2[(i / 2) % 4], f32x2(p0, p1));
     }
+    if (part == 0) pre_store();   // P's columns may still be read by the previous P V
     if constexpr (PF == PFmt::kE4m3) {
       // four keys per TMEM column
       uint32_t r[kKeys / 4];
@@ -374,6 +378,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   using G = Geo<D, FP8, PV16>;
   constexpr PFmt kPFmt = p_fmt<FP8, PV16>();
   constexpr int kPHalves = p_parts();
+  // Head dim 64 (not with the f16 P V product, whose converter warps need warps 10-11): O_h takes
+  // 64 of its 128 TMEM columns and P_h the other 64, so S_h is free again as soon as the softmax
+  // has read it, and each tile gets an issuing warp of its own (warps 9 and 10).  Measured on
+  // B1 H16 N32768 d64 causal: 1017 -> 1084 TFLOPS.  (The two tiles' softmaxes then run in phase
+  // and share MUFU; a single issuer polling both tiles without blocking measured 608: each probe
+  // is a shared-memory round trip, so it reacted ~2000 cycles late.)
+  constexpr bool kSepP = D == 64 && !G::kPv16;
   constexpr int kL2PrefetchBlocks = l2_prefetch_blocks<FP8>();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -415,17 +426,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&ctl->q_full), 1);
     for (int s = 0; s < G::kSlots; ++s) {
       mbar_init(smem_u32(&ctl->kv_full[s]), 1);
-      mbar_init(smem_u32(&ctl->kv_empty[s]), 1);
+      mbar_init(smem_u32(&ctl->kv_empty[s]), kSepP ? 2 : 1);   // head dim 64: one per tile
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(smem_u32(&ctl->s_full[h]), 1);
       for (int q = 0; q < p_parts(); ++q)
         mbar_init(smem_u32(&ctl->p_full[h][q]), 4);  // one arrival per softmax warp
       mbar_init(smem_u32(&ctl->o_full[h]), 1);
+      mbar_init(smem_u32(&ctl->s_read[h]), 4);   // one arrival per softmax warp
+      mbar_init(smem_u32(&ctl->pv_done[h]), 1);
       mbar_init(smem_u32(&ctl->v16_full[h]), 2);  // one arrival per converter warp
       mbar_init(smem_u32(&ctl->v16_empty[h]), 1);
     }
-    mbar_init(smem_u32(&ctl->drain), 1);
+    mbar_init(smem_u32(&ctl->drain), kSepP ? 2 : 1);   // head dim 64: one issuer per tile
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -502,8 +515,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ============================================================ MMA issuer
+  } else if (warp == kMmaWarp || (kSepP && warp == kMmaWarp + 1)) {
+    // ============================================================ MMA issuer(s)
     if (nkv_load > 0) {
       // The whole warp runs the issue loop, so the descriptor arithmetic is warp-uniform; one
       // lane, elected from the converged warp, issues each product and commit.  (With the loop
@@ -550,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int kN = G::kPvSteps / kPHalves;   // MMAs per published part of P
         // A: 8 TMEM columns of P per MMA; B: the next key group of V
         const uint32_t acc = (j > 0 || half > 0) ? 1u : 0u;
-        const uint32_t a_tm = tmem + h * 128 + half * kN * 8;
+        const uint32_t a_tm = tmem + (kSepP ? 256 + h * 128 + 64 : h * 128) + half * kN * 8;
         const uint64_t b_desc = vd + static_cast<uint64_t>(half * kN * G::kPvStep);
         if (issuer())
           mma_chain_ts_off<kN, G::kPE4m3 ? 1 : 0, G::kPvStep, 8, 16, 24, 32, 40, 48, 56>(
@@ -604,15 +617,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
 
       ok = ok && wait_kv(0);
-      if (ok) {
-        tc_fence_after();
-        if (nkv0 > 0) issue_s(0, 0);
-        if (nkv1 > 0) issue_s(1, 0);
-      }
-      for (int j = 0; j < nkv_load && ok; ++j) {
+      if constexpr (!kSepP) {
+        if (ok) {
+          tc_fence_after();
+          if (nkv0 > 0) issue_s(0, 0);
+          if (nkv1 > 0) issue_s(1, 0);
+        }
+        for (int j = 0; j < nkv_load && ok; ++j) {
 #pragma unroll
-        for (int h = 0; h < 2 && ok; ++h)
-          if (j < nkv[h]) ok = step(h, j);
+          for (int h = 0; h < 2 && ok; ++h)
+            if (j < nkv[h]) ok = step(h, j);
+        }
+      } else {
+        // Head dim 64: warp 9 issues tile 0's products and warp 10 tile 1's.  Per tile the events
+        // come in a fixed order -- the softmax reads S_h(j), then publishes the two parts of
+        // P_h(j) -- so each issuer waits for them one by one (blocking, bounded waits) and the
+        // two tiles never wait for each other.  S_h(j+1) goes in as soon as the softmax has
+        // read S_h(j); P V of block j as soon as its part of P_h(j) is published.  Ring slots
+        // go back by tcgen05.commit from each tile that reads them (two arrivals per slot; a
+        // tile alone on a block commits twice).
+        const int h = warp - kMmaWarp;
+        const int o = 1 - h;
+        auto commit_to = [&](uint32_t bar, int times) {
+          if (issuer())
+            for (int i = 0; i < times; ++i) tc_commit(bar);
+          __syncwarp();
+        };
+        if (ok && nkv[h] > 0) {
+          tc_fence_after();
+          issue_s(h, 0);
+          commit_to(smem_u32(&ctl->kv_empty[0]), 0 < nkv[o] ? 1 : 2);
+          for (int j = 0; j < nkv[h] && ok; ++j) {
+            const int tv = 2 * j + 1, tk = 2 * j + 2;
+            if (j + 1 < nkv[h]) {
+              ok = mwait(smem_u32(&ctl->s_read[h]), j & 1) && wait_kv(tk);
+              if (!ok) break;
+              tc_fence_after();
+              issue_s(h, j + 1);
+              commit_to(smem_u32(&ctl->kv_empty[tk % G::kSlots]), j + 1 < nkv[o] ? 1 : 2);
+            }
+            const uint64_t vd = smem_desc(ring_base + (tv % G::kSlots) * G::kTileBytes,
+                                          kTileRows * G::kPvSwBytes, 8 * G::kPvSwBytes,
+                                          G::kSwMode);
+#pragma unroll
+            for (int part = 0; part < kPHalves; ++part) {
+              ok = mwait(smem_u32(&ctl->p_full[h][part]), j & 1) && (part > 0 || wait_kv(tv));
+              if (!ok) break;
+              tc_fence_after();
+              if (part == 0) EXATTN_TRACE_EVENT(4, h, j);
+              issue_pv_part(h, j, part, vd);
+            }
+            if (!ok) break;
+            EXATTN_TRACE_EVENT(5, h, j);
+            commit_to(smem_u32(&ctl->pv_done[h]), 1);
+            if (j == nkv[h] - 1) commit_to(smem_u32(&ctl->o_full[h]), 1);
+            commit_to(smem_u32(&ctl->kv_empty[tv % G::kSlots]), j < nkv[o] ? 1 : 2);
+          }
+        }
       }
       // make sure nothing this thread issued is still running before TMEM is released
       __syncwarp();
@@ -686,8 +747,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r_local = w4 * 32 + lane;        // TMEM lane == row within the tile
     const int row = row0 + h * kTileRows + r_local;
     const uint32_t lane_addr = static_cast<uint32_t>(w4 * 32) << 16;
-    const uint32_t t_s = tmem + lane_addr + h * 128;        // S_h / P_h
+    const uint32_t t_s = tmem + lane_addr + h * 128;        // S_h
     const uint32_t t_o = tmem + lane_addr + 256 + h * 128;  // O_h
+    const uint32_t t_p = kSepP ? t_o + 64 : t_s;             // P_h (over S_h for head dim 128)
     float c = args.c;
     float m_run = -INFINITY;  // running max of scaled logits, log2 units
     float l_run = 0.f;        // running sum of 2^(x - m_run) (times 2^p_offset_log2)
@@ -737,7 +799,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // no rows) visits every loaded block, and its MMAs are issued after tile 0's, so S_h(j)
       // complete means both tiles are done with K_j, and (S_h(j) following P V of block j - 1)
       // with V_{j-1} (or its f16 copy).
-      if (threadIdx.x % 128 == 0 && h == (nkv1 > 0 ? 1 : 0)) {
+      // (head dim 64: the MMA warp hands the slots back itself)
+      if (!kSepP && threadIdx.x % 128 == 0 && h == (nkv1 > 0 ? 1 : 0)) {
         mbar_arrive(smem_u32(&ctl->kv_empty[(2 * j) % G::kSlots]));
         if (j > 0)
           mbar_arrive(smem_u32(G::kPv16 ? &ctl->v16_empty[(j - 1) & 1]
@@ -756,6 +819,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) s[cb * 32 + i] = __uint_as_float(r[cb][i]);
       }
+      if constexpr (kSepP) {
+        // S_h(j) is in registers: the MMA warp may compute S_h(j+1) over it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->s_read[h]));
+      }
+      // head dim 64: P V of block j - 1 must be complete before O_h is rescaled or P_h(j) is
+      // written over P_h(j - 1)
+      bool pv_prev_done = !kSepP || j == 0;
+      auto wait_pv_prev = [&]() {
+        if (pv_prev_done) return;
+        ok = __all_sync(0xffffffffu, wait_phase(smem_u32(&ctl->pv_done[h]), (j - 1) & 1,
+                                                abort_flag, args.status));
+        tc_fence_after();
+        pv_prev_done = true;
+      };
       // masks: keys past the end of the sequence, and the causal diagonal block
       const int jg = jb + j;  // block index within the head
       const int key0 = jg * kTileRows;
@@ -789,6 +868,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (j == 0) {
         m_run = m_cand;
       } else if (__any_sync(0xffffffffu, m_cand - m_run > rescale_log2<kPFmt>())) {
+        wait_pv_prev();
         const float alpha = ex2_mufu(m_run - m_cand);
         uint32_t r[32];
 #pragma unroll
@@ -826,9 +906,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         l_fix = fmaf(round_p<kPFmt>(p_top) - p_top, l_mult, l_fix);
       }
       const float rowsum =
-          masked ? exp_and_publish<true, kPFmt, kPHalves, 0>(s, c_j, m_shift, lim, t_s, pb0, lane)
-                 : exp_and_publish<false, kPFmt, kPHalves, EXATTN_EMU_EVERY>(s, c_j, m_shift, lim,
-                                                                             t_s, pb0, lane);
+          masked ? exp_and_publish<true, kPFmt, kPHalves, 0>(s, c_j, m_shift, lim, t_p, pb0, lane,
+                                                             wait_pv_prev)
+                 : exp_and_publish<false, kPFmt, kPHalves, EXATTN_EMU_EVERY>(
+                       s, c_j, m_shift, lim, t_p, pb0, lane, wait_pv_prev);
       if (threadIdx.x % 128 == 0) EXATTN_TRACE_EVENT(3, h, j);
       l_run = fmaf(rowsum, l_mult, l_run);
     }
