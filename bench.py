@@ -278,6 +278,9 @@ def sample_parity(o, lse, ref, dtype: str):
             "n_over_tol_o_plus_half_ulp": int((err > tol_o + half_ulp).sum())}
 
 
+L2_BYTES = 129e6          # GB300 L2 (about 126 MiB usable)
+FLUSH_BYTES = 256 << 20   # written between steps to evict inputs that fit in L2
+
 KERNEL_SOURCES = ["exact_attention_13_gb300/csrc/fa_fwd_kernel.cuh",
                   "exact_attention_13_gb300/csrc/sm103_ptx.cuh",
                   "exact_attention_13_gb300/csrc/fa_api.cu"]
@@ -438,19 +441,35 @@ def run_ours(args, w, world, rank, local):
 
             dist.barrier()
 
-    # ---- device-timed region: K launches back to back on one stream
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # ---- device-timed region: K launches back to back on one stream, or, when the inputs fit in
+    # L2, each launch timed on its own with a 256 MB write between launches that evicts them
+    in_l2 = 3 * q.numel() * q.element_size() <= L2_BYTES
     clk = NvmlClocks(dev)
     barrier()
     torch.cuda.synchronize()
-    with clk:
-        start.record(stream)
-        for _ in range(args.steps):
-            step()
-        end.record(stream)
-        torch.cuda.synchronize()
+    if not in_l2:
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with clk:
+            start.record(stream)
+            for _ in range(args.steps):
+                step()
+            end.record(stream)
+            torch.cuda.synchronize()
+        ms = start.elapsed_time(end) / args.steps
+    else:
+        flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        with clk:
+            for e0, e1 in evs:
+                flush.fill_(1)
+                e0.record(stream)
+                step()
+                e1.record(stream)
+            torch.cuda.synchronize()
+        ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / args.steps
+        del flush
     barrier()
-    ms = start.elapsed_time(end) / args.steps
     clocks = clk.summary()
     ms_max = max_over_ranks(ms, world, dev)
     assert ea.device_status() == 0, "device wait timed out during the bench"
@@ -560,9 +579,10 @@ def run_ours(args, w, world, rank, local):
     achieved = flops_rank / (ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak,
-                "traffic": measured_traffic(w.name, args.traffic_bytes, "_".join(
-                    ([("pv16" if pv16 else "")] if is_fp8 else []) + (["block"] if block else []))
-                    .strip("_")),
+                "traffic": None if args.lib else measured_traffic(
+                    w.name, args.traffic_bytes, "_".join(
+                        ([("pv16" if pv16 else "")] if is_fp8 else []) +
+                        (["block"] if block else [])).strip("_")),
                 "peak_kind": f"{pk['source']} cuBLAS bf16 burst" + peak_note,
                 "kernel": "exattn::fa_fwd_kernel"}
     # exp-unit bound at the clock seen during the run (informative)
@@ -581,8 +601,9 @@ def run_ours(args, w, world, rank, local):
                    "key_splits": args.splits,
                    **({"pv_product": args.fp8_pv, "fp8_scaling": args.fp8_scaling}
                       if is_fp8 else {}),
-                   "l2": "inputs larger than L2 (no flush)" if 3 * q.numel() * q.element_size()
-                   > 129e6 else "inputs smaller than L2"},
+                   **({"library": args.lib} if args.lib else {}),
+                   "l2": "inputs larger than L2 (no flush)" if not in_l2 else
+                   "inputs fit in L2: 256 MB written between steps, each step timed alone"},
         "pct_of_peak": 100.0 * achieved / peak,
         "exp_bound": {"exp_per_clk_sm": EXP_PER_CLK_SM, "floor_ms": exp_floor_ms,
                       "frac": exp_floor_ms / ms},
@@ -757,7 +778,17 @@ def main():
                     help="--op quantize: apply the incoherent (Hadamard) transform")
     ap.add_argument("--traffic-bytes", type=float, default=None,
                     help="DRAM bytes per launch from an ncu capture of the current kernel")
+    ap.add_argument("--lib", default=None,
+                    help="time this build of the library (e.g. a compile-time variant of the "
+                         "kernel) instead of the package's libexattn.so; the roofline's DRAM "
+                         "traffic is then null")
     args = ap.parse_args()
+    if args.lib:
+        if args.impl == "reference":
+            ap.error("--lib applies to --impl ours")
+        import exact_attention_13_gb300 as ea
+
+        ea.lib(os.path.abspath(args.lib))
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = WORKLOADS[args.workload]

@@ -105,6 +105,12 @@ constexpr float kLn2 = 0.6931471805599453f;
 #ifndef EXATTN_EMU_EVERY
 #define EXATTN_EMU_EVERY 0
 #endif
+// e4m3 P: exponentials two at a time by ex2.approx.f16x2 (unmasked blocks).  f16x2 ex2 runs at
+// half the instruction rate of f32 ex2 (the same 32 results/clk/SM), so it saves issue slots
+// but not MUFU time; off by default.
+#ifndef EXATTN_EX2_F16X2
+#define EXATTN_EX2_F16X2 0
+#endif
 
 // Format of the probabilities P handed to the P V product.
 enum class PFmt { kBf16, kF16, kE4m3 };
@@ -309,6 +315,50 @@ __device__ __forceinline__ float exp_and_publish(float (&s)[128], float c, float
                                                  PreStore&& pre_store) {
   static_assert(P_PARTS == 2, "P is published in two parts of 64 keys");
   constexpr int kKeys = 128 / P_PARTS;   // keys per published part
+#if EXATTN_EX2_F16X2
+  if constexpr (PF == PFmt::kE4m3 && !MASKED && EMU_EVERY == 0) {
+    // Two exponentials per MUFU instruction (ex2.approx.f16x2).  The argument leaves out P's
+    // 2^8 offset, so it is at most 0.8 and its f16 rounding stays below 2^-11 absolute; p is
+    // then scaled by 2^8 in f16 (exact) and converted to e4m3.  The row sum takes p pairwise in
+    // f16 (one rounding) and accumulates in fp32.
+    const float2 c2 = f32x2(c, c), nm2 = f32x2(-(m + 8.f), -(m + 8.f));
+    float2 ps2[4] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f), f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
+#pragma unroll
+    for (int part = 0; part < P_PARTS; ++part) {
+      uint32_t r[kKeys / 4];
+#pragma unroll
+      for (int q = 0; q < kKeys / 4; ++q) {
+        const int i = kKeys * part + 4 * q;
+        const float2 xa = fma_f32x2(f32x2(s[i], s[i + 1]), c2, nm2);
+        const float2 xb = fma_f32x2(f32x2(s[i + 2], s[i + 3]), c2, nm2);
+        uint32_t ha = pack_f16x2(f32x2_lo(xa), f32x2_hi(xa));
+        uint32_t hb = pack_f16x2(f32x2_lo(xb), f32x2_hi(xb));
+        ha = ex2_f16x2(ha);
+        hb = ex2_f16x2(hb);
+        r[q] = e4m3x4_from_f16x2_scaled256(ha, hb);
+        const uint32_t hs = hadd_f16x2(ha, hb);
+        ps2[q % 4] = add_f32x2(ps2[q % 4], f16x2_to_f32x2(hs));
+      }
+      if (part == 0) pre_store();
+      tmem_st16(t_s + 16 * part, r);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar0 + 8 * part);
+    }
+    float ps[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      ps[2 * k] = f32x2_lo(ps2[k]);
+      ps[2 * k + 1] = f32x2_hi(ps2[k]);
+    }
+#pragma unroll
+    for (int w = 4; w >= 1; w /= 2)
+#pragma unroll
+      for (int k = 0; k < w; ++k) ps[k] += ps[k + w];
+    return ps[0] * 256.f;
+  }
+#endif
   // eight partial sums (element i goes to sum i % 8), kept as four packed pairs; the exponent
   // arguments s c - m are formed two at a time (same rounding as the scalar fma)
   float2 ps2[4] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f), f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
@@ -911,7 +961,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // makes O exact for a single dominant key; the LSE keeps l_run.  (Without the lazy
       // rescale the row's largest probability is exactly 2^offset and needs no correction.)
       if constexpr (rescale_log2<kPFmt>() > 0.f) {
-        const float p_top = ex2_mufu(fmaf(mp[0], c_j, -m_shift));
+        float p_top = ex2_mufu(fmaf(mp[0], c_j, -m_shift));
+#if EXATTN_EX2_F16X2
+        // unmasked e4m3 blocks take p through f16 (see exp_and_publish)
+        if (kPFmt == PFmt::kE4m3 && !masked) {
+          const float x = fmaf(mp[0], c_j, -(m_shift + 8.f));
+          p_top = f16x2_to_f32x2(ex2_f16x2(pack_f16x2(x, x))).x * 256.f;
+        }
+#endif
         l_fix = fmaf(round_p<kPFmt>(p_top) - p_top, l_mult, l_fix);
       }
       const float rowsum =

@@ -532,6 +532,46 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return r;
 }
 
+// 2^x for both halves of an f16x2 (MUFU, two results per instruction).
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// Sum of two f16x2, element by element (round to nearest even).
+__device__ __forceinline__ uint32_t hadd_f16x2(uint32_t a, uint32_t b) {
+  uint32_t y;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(y) : "r"(a), "r"(b));
+  return y;
+}
+
+// The two halves of an f16x2 as fp32 (exact): bits 0-15 -> .x, bits 16-31 -> .y.
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t h) {
+  float lo, hi;
+  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h));
+  return make_float2(lo, hi);
+}
+
+// Four f16 values (a: bits 0-15 -> byte 0, bits 16-31 -> byte 1; b likewise -> bytes 2-3) times
+// 2^8 (exact in f16), rounded to e4m3 (nearest even, saturating).
+__device__ __forceinline__ uint32_t e4m3x4_from_f16x2_scaled256(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("{\n\t.reg .b32 sa, sb, k;\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 k, 0x5C005C00;\n\t"
+      "mul.rn.f16x2 sa, %1, k;\n\t"
+      "mul.rn.f16x2 sb, %2, k;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f16x2 lo, sa;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f16x2 hi, sb;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "r"(a), "r"(b));
+  return r;
+}
+
 // Widen two e4m3 values (byte 0 -> bits 0-15, byte 1 -> bits 16-31) to f16x2; exact, since
 // every e4m3 value is an f16 value.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {

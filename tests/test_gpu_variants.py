@@ -33,6 +33,7 @@ VARIANTS = {
     "emu2": ["-DEXATTN_EMU_EVERY=2"],
     "rescale0": ["-DEXATTN_RESCALE_LOG2=0.0f"],
     "ring5_pf4": ["-DEXATTN_KV_SLOTS_D128=5", "-DEXATTN_L2_PREFETCH_BLOCKS=4"],
+    "ex2f16x2": ["-DEXATTN_EX2_F16X2=1"],
 }
 
 
