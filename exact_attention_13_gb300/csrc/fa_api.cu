@@ -60,10 +60,11 @@ int* library_status_ptr(int dev) {
   return static_cast<int*>(addr);
 }
 
-// [B*H, N, d] view of one operand, tiles of 128 rows x (one swizzle span) with the swizzle the
-// MMA descriptors expect.  Rows past N (per head) read as zero.
+// [B*H, N, d] view of one operand, tiles of box_rows (128) rows x (one swizzle span) with the
+// swizzle the MMA descriptors expect.  Rows past N (per head) read as zero (loads) or are clipped
+// (stores).
 bool encode_operand_map(CUtensorMap* map, const void* ptr, int elem_bytes, int d, int n,
-                        int bh) {
+                        int bh, int box_rows = 128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const int row_bytes = d * elem_bytes;
@@ -72,7 +73,8 @@ bool encode_operand_map(CUtensorMap* map, const void* ptr, int elem_bytes, int d
                         static_cast<cuuint64_t>(bh)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_bytes),
                            static_cast<cuuint64_t>(row_bytes) * static_cast<cuuint64_t>(n)};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(sw_bytes / elem_bytes), 128, 1};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(sw_bytes / elem_bytes),
+                       static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                        : CU_TENSOR_MAP_DATA_TYPE_UINT8,
@@ -96,10 +98,12 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
            float c, float out_mult, int* status, int splits, float* o_part, float* lse_part,
            const BlockScales* bs, int mblock0, int mblocks, cudaStream_t stream) {
   constexpr int elem = FP8 ? 1 : 2;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   const int bh = B * H;
+  // O (bf16 for every operand type): boxes of one softmax warp's 32 rows, for the bulk-store
+  // epilogue
   if (!encode_operand_map(&mq, q, elem, D, N, bh) || !encode_operand_map(&mk, k, elem, D, N, bh) ||
-      !encode_operand_map(&mv, v, elem, D, N, bh))
+      !encode_operand_map(&mv, v, elem, D, N, bh) || !encode_operand_map(&mo, o, 2, D, N, bh, 32))
     return FA_ERR_CUDA;
   auto kern = fa_fwd_kernel<D, FP8, CAUSAL, PV16>;
   constexpr int smem = smem_bytes<D, FP8, PV16>();
@@ -135,7 +139,7 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   const unsigned z = static_cast<unsigned>(splits);
   const dim3 grid = CAUSAL ? dim3(static_cast<unsigned>(bh), mb, z)
                            : dim3(mb, static_cast<unsigned>(bh), z);
-  kern<<<grid, kThreads, smem_request, stream>>>(mq, mk, mv, args);
+  kern<<<grid, kThreads, smem_request, stream>>>(mq, mk, mv, mo, args);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
