@@ -240,9 +240,13 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
                const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, float scale,
                float* delta, int* status, cudaStream_t stream) {
   const int bh = B * H;
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
+  // outputs: boxes of one softmax warp's 32 rows, for the bulk-store epilogues
   if (!encode_operand_map(&mq, q, 2, D, N, bh) || !encode_operand_map(&mk, k, 2, D, N, bh) ||
-      !encode_operand_map(&mv, v, 2, D, N, bh) || !encode_operand_map(&mdo, dout, 2, D, N, bh))
+      !encode_operand_map(&mv, v, 2, D, N, bh) || !encode_operand_map(&mdo, dout, 2, D, N, bh) ||
+      !encode_operand_map(&mdq, dq, 2, D, N, bh, 32) ||
+      !encode_operand_map(&mdk, dk, 2, D, N, bh, 32) ||
+      !encode_operand_map(&mdv, dv, 2, D, N, bh, 32))
     return FA_ERR_CUDA;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
@@ -273,11 +277,11 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   const dim3 grid = CAUSAL ? dim3(static_cast<unsigned>(bh), nblk) : dim3(nblk, static_cast<unsigned>(bh));
   a.g0 = static_cast<__nv_bfloat16*>(dk);
   a.g1 = static_cast<__nv_bfloat16*>(dv);
-  kkv<<<grid, kBwdThreads, smem_request, stream>>>(mq, mk, mv, mdo, a);
+  kkv<<<grid, kBwdThreads, smem_request, stream>>>(mq, mk, mv, mdo, mdk, mdv, a);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   a.g0 = static_cast<__nv_bfloat16*>(dq);
   a.g1 = nullptr;
-  kq<<<grid, kBwdThreads, smem_dq_request, stream>>>(mq, mk, mv, mdo, a);
+  kq<<<grid, kBwdThreads, smem_dq_request, stream>>>(mq, mk, mv, mdo, mdq, a);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -264,6 +264,7 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
+                    const __grid_constant__ CUtensorMap map_g0, const __grid_constant__ CUtensorMap map_g1,
                     const BwdArgs args) {
   using G = BwdGeo<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -503,7 +504,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = wait_phase(smem_u32(&ctl->o_full), 0, abort_flag, status);
       ok = __all_sync(0xffffffffu, ok);
     }
-    if (ok) {
+    if (ok && D == 128) {
+      // Bulk-store epilogue (head dim 128): the warp's 32 key rows x 64 columns of dV and dK,
+      // rounded to bf16, go into the V and K tiles (free: every product has completed) in the
+      // 128-byte-swizzled layout of the output tensor maps' boxes, and one lane stores them
+      // (rows past N are clipped by the maps).
+      tc_fence_after();
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {   // 0: dV (cols 256..), 1: dK (cols 384..)
+        const uint32_t t_acc = tmem + lane_addr + (which ? 384 : 256) + G::kHalfCols * hc;
+        const float mult = which ? args.scale : 1.f;
+        uint32_t rr[2][32];
+        tmem_ld32(t_acc, rr[0]);
+        tmem_ld32(t_acc + 32, rr[1]);
+        tmem_ld_wait();
+        const uint32_t box = smem_u32(which ? s_k : s_v) + hc * (kTileRows * 128);
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {   // 16-byte chunk (8 columns) of the row's 64
+          uint32_t pk[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(rr[g / 4][8 * (g % 4) + 2 * i]) * mult,
+                                __uint_as_float(rr[g / 4][8 * (g % 4) + 2 * i + 1]) * mult);
+          st_shared_v4(box + r * 128 + ((g ^ (r & 7)) * 16), pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      const int wrow = jblk * kTileRows + w4 * 32;   // the warp's first key row
+      if (lane == 0 && wrow < n) {
+        const uint32_t slab = hc * (kTileRows * 128) + w4 * 32 * 128;
+        tma_store_3d(&map_g1, smem_u32(s_v) + slab, 64 * hc, wrow, bh);
+        tma_store_3d(&map_g0, smem_u32(s_k) + slab, 64 * hc, wrow, bh);
+        bulk_commit_group();
+        bulk_wait_group_read0();   // the CTA's shared memory must outlive the reads
+      }
+      __syncwarp();
+    } else if (ok) {
       tc_fence_after();
       const bool live = key < n;
       const size_t row_off = (static_cast<size_t>(bh) * n + (live ? key : 0)) * D + G::kHalfCols * hc;
@@ -549,7 +586,7 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
-                  const BwdArgs args) {
+                  const __grid_constant__ CUtensorMap map_g0, const BwdArgs args) {
   using G = BwdGeo<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -760,7 +797,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = wait_phase(smem_u32(&ctl->o_full), 0, abort_flag, status);
       ok = __all_sync(0xffffffffu, ok);
     }
-    if (ok) {
+    if (ok && D == 128) {
+      // bulk-store epilogue, as in the dK/dV kernel: the warp's rows of dQ through the Q tile
+      tc_fence_after();
+      const uint32_t t_acc = tmem + lane_addr + 256 + G::kHalfCols * hc;
+      uint32_t rr[2][32];
+      tmem_ld32(t_acc, rr[0]);
+      tmem_ld32(t_acc + 32, rr[1]);
+      tmem_ld_wait();
+      const uint32_t box = smem_u32(s_q) + hc * (kTileRows * 128);
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          pk[i] = pack_bf16x2(__uint_as_float(rr[g / 4][8 * (g % 4) + 2 * i]) * args.scale,
+                              __uint_as_float(rr[g / 4][8 * (g % 4) + 2 * i + 1]) * args.scale);
+        st_shared_v4(box + r * 128 + ((g ^ (r & 7)) * 16), pk[0], pk[1], pk[2], pk[3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      const int wrow = iblk * kTileRows + w4 * 32;   // the warp's first query row
+      if (lane == 0 && wrow < n) {
+        tma_store_3d(&map_g0, box + w4 * 32 * 128, 64 * hc, wrow, bh);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+      }
+      __syncwarp();
+    } else if (ok) {
       tc_fence_after();
       const uint32_t t_acc = tmem + lane_addr + 256 + G::kHalfCols * hc;
       __nv_bfloat16* dst = args.g0 + ridx * D + G::kHalfCols * hc;
