@@ -281,6 +281,13 @@ def sample_parity(o, lse, ref, dtype: str):
 L2_BYTES = 129e6          # GB300 L2 (about 126 MiB usable)
 FLUSH_BYTES = 256 << 20   # written between steps to evict inputs that fit in L2
 
+def inputs_fit_in_l2(w) -> bool:
+    """Whether the workload's Q, K and V together fit in L2 (then each timed launch is preceded
+    by a write that evicts them)."""
+    elem = 1 if w.dtype == "e4m3" else 2
+    return 3 * w.B * w.H * w.N * w.d * elem <= L2_BYTES
+
+
 KERNEL_SOURCES = ["exact_attention_13_gb300/csrc/fa_fwd_kernel.cuh",
                   "exact_attention_13_gb300/csrc/sm103_ptx.cuh",
                   "exact_attention_13_gb300/csrc/fa_api.cu"]
@@ -443,7 +450,7 @@ def run_ours(args, w, world, rank, local):
 
     # ---- device-timed region: K launches back to back on one stream, or, when the inputs fit in
     # L2, each launch timed on its own with a 256 MB write between launches that evicts them
-    in_l2 = 3 * q.numel() * q.element_size() <= L2_BYTES
+    in_l2 = inputs_fit_in_l2(w)
     clk = NvmlClocks(dev)
     barrier()
     torch.cuda.synchronize()
