@@ -59,7 +59,7 @@ class NvmlClocks:
     REASON_BITS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
                    0x4: "sw_power_cap"}
 
-    def __init__(self, device, period_s: float = 0.002):
+    def __init__(self, device, period_s: float = 0.001):
         import ctypes
         import threading
 
